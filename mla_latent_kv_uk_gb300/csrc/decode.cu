@@ -1,0 +1,774 @@
+// A3/A4/A5: split-KV plan, paged latent decode (forward_mqa) and the
+// on-device merge of split partials.
+//
+// Sources: prhub digest of vLLM PR 44044, §关键源码片段 mla_attention.py
+// (forward_mqa(mqa_q, kv_cache, attn_metadata) -> attn_out, lse) and
+// §关键源码片段 flashmla.py (split scheduler metadata derived on the device
+// from seq_lens and the true head count); "DeepSeek MLA 在 DCP 分布式环境中的
+// Prefill 阶段解析", §MLA Prefill vs Decode (decode keeps KV as one latent
+// head of width 512 + 64; the value is the 512-wide latent part) and
+// §Chunked Prefill 与 LSE Merge (LSE-rescaling merge of partial states).
+//
+// Design (GB300, sm_103a):
+//  * All 128 heads of a query token share one latent KV row, so per 32-token
+//    tile S = Q K^T is a dense [128 x 32 x 576] contraction and O += P V a
+//    [128 x 256 x 32] one: both run on tcgen05 with fp32 TMEM accumulators.
+//  * The fp32 output of 128 heads x 512 latent columns is exactly one SM's
+//    TMEM, so each work span is processed by a PAIR of CTAs: CTA c owns
+//    latent columns [256c, 256c + 256) of O and recomputes S itself (the
+//    two CTAs read the same KV tiles; the second read is an L2 hit).
+//  * TMEM (512 columns): O half [0,256), S/P double buffer [256,320),
+//    query dims 0..383 as the MMA A operand [320,512).  Query dims
+//    384..575 stay in shared memory; the KV ring holds 4 tiles of 36 KB.
+//  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer (+ TMEM owner),
+//    warps 2..5 online softmax (one head row per thread), correction and
+//    epilogue.  Lazy rescaling: O is rescaled only when a row max grows by
+//    more than 2^8.
+//  * Work split (A3): every job (request, query token, 128-head group)
+//    contributes the 32-token tiles its key range touches; jobs are laid
+//    end to end and CTA pair p takes flat tiles [p*C, (p+1)*C).  A job cut
+//    into several spans writes fp32 partials that a merge kernel combines.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "merge_row.cuh"
+#include "sm100.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kTile = 32;                    // tokens per KV tile
+constexpr int kStages = 4;                   // KV ring depth
+constexpr int kBox = kTile * 128;            // one 32 x 64 bf16 box, 4 KB
+constexpr int kStageBytes = 9 * kBox;        // 576 columns, 36 KB
+constexpr int kQBox = 128 * 128;             // 128 rows x 64 bf16, 16 KB
+constexpr int kQsBoxes = 3;                  // query dims 384..575
+constexpr int kQtCols = 192;                 // query dims 0..383 in TMEM
+constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
+constexpr int kThreads = 192;
+constexpr int kMinTiles = 4;                 // smallest auto span
+constexpr float kRescaleLog2 = 8.f;          // lazy rescale threshold
+
+constexpr int kSmemQ = 0;
+constexpr int kSmemKV = kQsBoxes * kQBox;                    // 48 KB
+constexpr int kSmemBar = kSmemKV + kStages * kStageBytes;    // 192 KB
+constexpr int kSmemBytes = kSmemBar + 256 + 1024;            // + align slack
+
+// ----------------------------------------------------------------- planner
+// Plan layout (int32): [0] total tiles, [1] C, [2] J, [3] spans, then
+// tile_prefix[J+1], seg_prefix[J+1], job_lo[J+1], job_hi[J+1].
+struct PlanView {
+  const int32_t *base;
+  int J;
+  __device__ int total() const { return base[0]; }
+  __device__ int chunk() const { return base[1]; }
+  __device__ const int32_t *tile_prefix() const { return base + 4; }
+  __device__ const int32_t *seg_prefix() const { return base + 4 + (J + 1); }
+  __device__ const int32_t *job_lo() const { return base + 4 + 2 * (J + 1); }
+  __device__ const int32_t *job_hi() const { return base + 4 + 3 * (J + 1); }
+};
+
+size_t plan_ints(int J) { return 4 + 4 * static_cast<size_t>(J + 1); }
+
+constexpr int kPlanThreads = 1024;
+
+// Exclusive prefix sum over n values held in v[0..n) (in place), one CTA.
+__device__ int block_exclusive_scan(int32_t *v, int n, int32_t *scratch) {
+  const int tid = threadIdx.x;
+  const int per = (n + kPlanThreads - 1) / kPlanThreads;
+  const int a = min(n, tid * per), z = min(n, a + per);
+  int local = 0;
+  for (int k = a; k < z; ++k) local += v[k];
+  // inclusive scan of `local` across the block
+  int x = local;
+  const int lane = tid & 31, warp = tid >> 5;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) scratch[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = scratch[lane];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    scratch[lane] = w;
+  }
+  __syncthreads();
+  int run = x - local + (warp ? scratch[warp - 1] : 0);
+  const int total = scratch[31];
+  for (int k = a; k < z; ++k) {
+    const int t = v[k];
+    v[k] = run;
+    run += t;
+  }
+  __syncthreads();
+  return total;
+}
+
+__global__ void __launch_bounds__(kPlanThreads)
+plan_kernel(const int32_t *__restrict__ seq_lens,
+            const int32_t *__restrict__ kv_starts,
+            const int32_t *__restrict__ kv_ends, int B, int q_len, int HG,
+            int max_blocks, int causal, int forced_chunk, int groups,
+            int32_t *plan, int *err) {
+  __shared__ int32_t scratch[32];
+  const int J = B * q_len * HG;
+  int32_t *tp = plan + 4;
+  int32_t *sp = tp + (J + 1);
+  int32_t *lo_a = sp + (J + 1);
+  int32_t *hi_a = lo_a + (J + 1);
+  for (int j = threadIdx.x; j < J; j += blockDim.x) {
+    const int bi = j / HG;
+    const int b = bi / q_len, i = bi % q_len;
+    int len = seq_lens[b];
+    if (len < 0 || len > max_blocks * kPage) {
+      if ((j % (q_len * HG)) == 0) raise_error(err, MLA_DEVERR_SEQ_LEN);
+      len = min(max(len, 0), max_blocks * kPage);
+    }
+    int hi = causal ? len - q_len + i + 1 : len;
+    hi = min(hi, len);
+    int lo = 0;
+    if (kv_starts) lo = max(lo, kv_starts[b]);
+    if (kv_ends) hi = min(hi, kv_ends[b]);
+    hi = max(hi, 0);
+    lo = min(max(lo, 0), hi);
+    lo_a[j] = lo;
+    hi_a[j] = hi;
+    tp[j] = hi > lo ? (hi + kTile - 1) / kTile - lo / kTile : 0;
+  }
+  if (threadIdx.x == 0) { lo_a[J] = 0; hi_a[J] = 0; }
+  __syncthreads();
+  const int total = block_exclusive_scan(tp, J, scratch);
+  if (threadIdx.x == 0) tp[J] = total;
+  const int C = forced_chunk > 0 ? forced_chunk
+                                 : max(kMinTiles, (total + groups - 1) / groups);
+  __syncthreads();
+  for (int j = threadIdx.x; j < J; j += blockDim.x) {
+    const int a = tp[j], z = tp[j + 1];
+    sp[j] = z > a ? (z - 1) / C - a / C + 1 : 0;
+  }
+  __syncthreads();
+  const int segs = block_exclusive_scan(sp, J, scratch);
+  if (threadIdx.x == 0) {
+    sp[J] = segs;
+    plan[0] = total;
+    plan[1] = C;
+    plan[2] = J;
+    plan[3] = (total + C - 1) / C;
+  }
+}
+
+// ---------------------------------------------------------- segment walk
+struct Seg {
+  int job, row0;        // job index, first q row ((b*q_len + i)*H + hg*128)
+  int b, hrows;         // request, valid head rows in this group
+  int out_row0;         // first output row ((b*q_len + i)*H + hg*128)
+  int lo, hi;           // key range
+  int tile0, ntiles;    // first absolute tile, tiles in this segment
+  int whole, slot;      // covers the whole job?  partial slot otherwise
+};
+
+struct SegWalk {
+  PlanView plan;
+  int q_len, H, HG, groups;
+  int p, span_lo, span_hi, j;
+  bool started;
+
+  __device__ void init(const int32_t *pl, int J, int ql, int h, int hg,
+                       int g, int group_id) {
+    plan = PlanView{pl, J};
+    q_len = ql; H = h; HG = hg; groups = g;
+    p = group_id;
+    started = false;
+  }
+
+  // Advances to the next segment of this CTA pair; false when done.
+  __device__ bool next(Seg &s) {
+    const int total = plan.total(), C = plan.chunk();
+    const int32_t *tp = plan.tile_prefix();
+    while (true) {
+      if (!started) {
+        if (p * C >= total) return false;
+        span_lo = p * C;
+        span_hi = min(total, span_lo + C);
+        // first job whose tiles contain span_lo
+        int a = 0, z = plan.J;  // last j with tp[j] <= span_lo
+        while (a < z) {
+          int mid = (a + z + 1) >> 1;
+          if (tp[mid] <= span_lo) a = mid; else z = mid - 1;
+        }
+        j = a;
+        started = true;
+      }
+      if (j >= plan.J || tp[j] >= span_hi) {
+        p += groups;
+        started = false;
+        continue;
+      }
+      const int a = tp[j], z = tp[j + 1];
+      if (z <= a) { ++j; continue; }  // empty job
+      const int u0 = max(span_lo, a), u1 = min(span_hi, z);
+      s.job = j;
+      const int bi = j / HG, hg = j % HG;
+      s.b = bi / q_len;
+      s.row0 = bi * H + hg * 128;
+      s.out_row0 = s.row0;
+      s.hrows = min(128, H - hg * 128);
+      s.lo = plan.job_lo()[j];
+      s.hi = plan.job_hi()[j];
+      s.tile0 = s.lo / kTile + (u0 - a);
+      s.ntiles = u1 - u0;
+      s.whole = (span_lo <= a) && (z <= span_hi);
+      s.slot = plan.seg_prefix()[j] + (span_lo / C - a / C);
+      ++j;
+      return true;
+    }
+  }
+};
+
+struct DecodeArgs {
+  const int32_t *plan;
+  int J;
+  const int32_t *block_table;
+  const int32_t *seq_lens;
+  const __nv_bfloat16 *q;     // [B, q_len, H, 576]
+  int q_len, H, HG, max_blocks, num_blocks, groups;
+  float scale_log2;
+  void *out;
+  int out_dtype;
+  float *lse;
+  float *ws_o;                // [slots, 128, 512]
+  float *ws_lse;              // [slots, 128]
+  int *err;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
+  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
+  const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
+  return lo | (hi << 16);
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
+                   const __grid_constant__ CUtensorMap tm_q, DecodeArgs args) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sm_q = smem + kSmemQ;
+  uint8_t *sm_kv = smem + kSmemKV;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemBar);
+  uint64_t *kv_full = bars;                 // [kStages]
+  uint64_t *kv_empty = bars + kStages;      // [kStages]
+  uint64_t *s_full = bars + 2 * kStages;    // [2]
+  uint64_t *p_full = s_full + 2;            // [2]
+  uint64_t *pv_done = p_full + 2;
+  uint64_t *q_full = pv_done + 1;
+  uint64_t *q_tmem = q_full + 1;
+  uint64_t *q_free = q_tmem + 1;
+  uint64_t *drain = q_free + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int half = blockIdx.x & 1;
+  const int group = blockIdx.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+    }
+    mbar_init(pv_done, 1);
+    mbar_init(q_full, 1);
+    mbar_init(q_tmem, 128);
+    mbar_init(q_free, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  SegWalk walk;
+  walk.init(args.plan, args.J, args.q_len, args.H, args.HG, args.groups, group);
+  Seg sg;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------ TMA producer
+      prefetch_tmap(&tm_kv);
+      prefetch_tmap(&tm_q);
+      int kc = 0, nseg = 0;
+      bool ok = true;
+      // Loads KV tile `tile` of request row `bt` into ring slot kc % kStages.
+      auto load_tile = [&](const int32_t *bt, int tile) -> bool {
+        const int s = kc % kStages;
+        if (kc >= kStages && !mbar_wait(&kv_empty[s], ((kc / kStages) - 1) & 1, abort_flag))
+          return false;
+        const int blk = __ldg(bt + tile / 2);
+        int row;
+        if (blk < 0 || blk >= args.num_blocks) {
+          raise_error(args.err, MLA_DEVERR_BLOCK_ID);
+          row = args.num_blocks * kPage;  // out of range: TMA fills zeros
+        } else {
+          row = blk * kPage + (tile & 1) * kTile;
+        }
+        uint8_t *dst = sm_kv + s * kStageBytes;
+        mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+        for (int d = 0; d < 9; ++d)
+          tma_load_2d(dst + d * kBox, &tm_kv, &kv_full[s], 64 * d, row);
+        ++kc;
+        return true;
+      };
+      while (ok && walk.next(sg)) {
+        const int32_t *bt = args.block_table + static_cast<int64_t>(sg.b) * args.max_blocks;
+        // The first ring-full of this segment's tiles only needs free ring
+        // slots; the query slot frees when the previous segment's MMAs end.
+        const int pre = min(sg.ntiles, kStages);
+        for (int t = 0; ok && t < pre; ++t) ok = load_tile(bt, sg.tile0 + t);
+        if (!ok) break;
+        if (nseg > 0 && !(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
+        mbar_arrive_expect_tx(q_full, kQsBoxes * kQBox);
+        for (int k = 0; k < kQsBoxes; ++k)
+          tma_load_2d(sm_q + k * kQBox, &tm_q, q_full, 384 + 64 * k, sg.row0);
+        ++nseg;
+        for (int t = pre; ok && t < sg.ntiles; ++t) ok = load_tile(bt, sg.tile0 + t);
+      }
+      if (*abort_flag) {
+        volatile int no_abort = 0;
+        for (int k = max(0, kc - kStages); k < kc; ++k)
+          mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &no_abort);
+        if (nseg > 0) mbar_wait(q_full, (nseg - 1) & 1, &no_abort);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t idesc_qk = idesc_bf16(128, kTile, false, false);
+      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      const uint32_t q_base = smem_u32(sm_q);
+      int kc = 0, uc = 0, nseg = 0;
+      bool ok = true;
+      auto issue_qk = [&](int kcx, int ucx) {
+        const uint32_t stage = smem_u32(sm_kv + (kcx % kStages) * kStageBytes);
+        const uint32_t d = tmem + kColS + 32 * (ucx & 1);
+#pragma unroll 4
+        for (int k = 0; k < 36; ++k) {
+          const uint64_t bdesc =
+              sdesc(stage + (k >> 2) * kBox + (k & 3) * 32, 16, 1024, kSwizzle128B);
+          if (k < 24) {
+            mma_f16_ts(d, tmem + kColQ + 8 * k, bdesc, idesc_qk, k > 0);
+          } else {
+            const int kq = k - 24;
+            const uint64_t adesc = sdesc(q_base + (kq >> 2) * kQBox + (kq & 3) * 32,
+                                         16, 1024, kSwizzle128B);
+            mma_f16_ss(d, adesc, bdesc, idesc_qk, 1);
+          }
+        }
+        mma_commit(&s_full[ucx & 1]);
+      };
+      while (ok && walk.next(sg)) {
+        // the query of this segment: smem part by TMA, TMEM part by softmax warps
+        ok = mbar_wait(q_full, nseg & 1, abort_flag) &&
+             mbar_wait(q_tmem, nseg & 1, abort_flag);
+        if (!ok) break;
+        ++nseg;
+        ok = mbar_wait(&kv_full[kc % kStages], (kc / kStages) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        issue_qk(kc, uc);
+        for (int t = 0; t < sg.ntiles; ++t, ++kc, ++uc) {
+          if (t + 1 < sg.ntiles) {
+            ok = mbar_wait(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(kc + 1, uc + 1);
+          }
+          ok = mbar_wait(&p_full[uc & 1], (uc >> 1) & 1, abort_flag);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t stage = smem_u32(sm_kv + (kc % kStages) * kStageBytes);
+#pragma unroll
+          for (int kk = 0; kk < 2; ++kk) {
+            const uint64_t bdesc = sdesc(stage + (4 * half) * kBox + kk * 2048,
+                                         kBox, 1024, kSwizzle128B);
+            mma_f16_ts(tmem + kColO, tmem + kColS + 32 * (uc & 1) + 8 * kk, bdesc,
+                       idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+          }
+          mma_commit(&kv_empty[kc % kStages]);
+          mma_commit(pv_done);
+          if (t + 1 == sg.ntiles) mma_commit(q_free);
+        }
+      }
+      if (!ok) {
+        mma_commit(drain);
+        volatile int no_abort = 0;
+        mbar_wait(drain, 0, &no_abort);
+      }
+    }
+  } else {
+    // -------------------------------------------- softmax / epilogue
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;  // head row within the group
+    const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
+    const int tid = threadIdx.x - 64;   // 0..127
+    int uc = 0, npv = 0, nseg = 0;
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      // query dims 0..383 of row r -> TMEM columns [kColQ, kColQ + 192)
+      {
+        const uint4 *src = reinterpret_cast<const uint4 *>(
+            args.q + static_cast<int64_t>(sg.row0 + r) * kDqk);
+        const bool valid = r < sg.hrows;
+#pragma unroll 1
+        for (int c = 0; c < kQtCols / 32; ++c) {
+          uint32_t w[32];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            uint4 v = valid ? __ldg(src + c * 8 + k) : make_uint4(0, 0, 0, 0);
+            w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+          }
+          tmem_st_x32(lane_base + kColQ + 32 * c, w);
+        }
+        tc_fence_before();
+        mbar_arrive(q_tmem);
+      }
+      ++nseg;
+      float m = -INFINITY, l = 0.f;
+      const int len = __ldg(args.seq_lens + sg.b);
+      for (int t = 0; t < sg.ntiles; ++t, ++uc) {
+        const int sb = uc & 1;
+        ok = mbar_wait(&s_full[sb], (uc >> 1) & 1, abort_flag);
+        if (!ok) break;
+        tc_fence_after();
+        uint32_t sr[32];
+        tmem_ld_x32(lane_base + kColS + 32 * sb, sr);
+        const int pos0 = (sg.tile0 + t) * kTile;
+        float x[32];
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+          const int pos = pos0 + jj;
+          const bool valid = pos >= sg.lo && pos < sg.hi;
+          x[jj] = valid ? __uint_as_float(sr[jj]) * args.scale_log2 : -INFINITY;
+          tmax = fmaxf(tmax, x[jj]);
+        }
+        if (t > 0) {
+          ok = mbar_wait(pv_done, npv & 1, abort_flag);
+          ++npv;
+          if (!ok) break;
+          tc_fence_after();
+          const float m_new = fmaxf(m, tmax);
+          const bool need = m_new > m + kRescaleLog2;
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? exp2f(m - m_new) : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < 256; c += 32) {
+              uint32_t o[32];
+              tmem_ld_x32(lane_base + kColO + c, o);
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st_x32(lane_base + kColO + c, o);
+            }
+            l *= alpha;
+            if (need) m = m_new;
+          }
+        } else {
+          m = tmax;
+        }
+        uint32_t pk[16];
+        float psum = 0.f;
+#pragma unroll
+        for (int jj = 0; jj < 16; ++jj) {
+          const float p0 = exp2f(x[2 * jj] - m);
+          const float p1 = exp2f(x[2 * jj + 1] - m);
+          pk[jj] = pack_bf16(p0, p1);
+          psum += __uint_as_float(pk[jj] << 16) + __uint_as_float(pk[jj] & 0xFFFF0000u);
+        }
+        l += psum;
+        tmem_st_x16(lane_base + kColS + 32 * sb, pk);
+        if (pos0 + kTile > len) {
+          // Cache rows past seq_len may hold anything (even NaN bits): zero
+          // this CTA's value columns of those rows so that P = 0 really
+          // contributes nothing to O.  The tile sits in ring stage
+          // uc % kStages (the producer fills stages in the same order).
+          const int first = max(0, len - pos0);
+          const int nrows = kTile - first;
+          uint8_t *vbase = sm_kv + (uc % kStages) * kStageBytes + (4 * half) * kBox;
+          for (int idx = tid; idx < nrows * 32; idx += 128) {
+            const int box = idx / (nrows * 8);
+            const int rem = idx - box * nrows * 8;
+            reinterpret_cast<uint4 *>(vbase + box * kBox + (first + rem / 8) * 128)[rem % 8] =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(&p_full[sb]);
+      }
+      if (!ok) break;
+      ok = mbar_wait(pv_done, npv & 1, abort_flag);
+      ++npv;
+      if (!ok) break;
+      tc_fence_after();
+      // ---- epilogue: O / l for this CTA's 256 latent columns
+      const float inv = 1.f / l;
+      const bool row_ok = r < sg.hrows;
+      const int64_t orow = static_cast<int64_t>(sg.out_row0 + r);
+#pragma unroll 1
+      for (int c = 0; c < 256; c += 32) {
+        uint32_t o[32];
+        tmem_ld_x32(lane_base + kColO + c, o);
+        if (!row_ok) continue;
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
+        const int col = 256 * half + c;
+        if (sg.whole) {
+          if (args.out_dtype == MLA_BF16) {
+            uint4 *dst = reinterpret_cast<uint4 *>(
+                static_cast<__nv_bfloat16 *>(args.out) + orow * kLatent + col);
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              dst[k] = make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]),
+                                  pack_bf16(v[8 * k + 2], v[8 * k + 3]),
+                                  pack_bf16(v[8 * k + 4], v[8 * k + 5]),
+                                  pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+          } else {
+            float4 *dst = reinterpret_cast<float4 *>(
+                static_cast<float *>(args.out) + orow * kLatent + col);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+          }
+        } else {
+          float4 *dst = reinterpret_cast<float4 *>(
+              args.ws_o + (static_cast<int64_t>(sg.slot) * 128 + r) * kLatent + col);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
+      }
+      if (row_ok && half == 0) {
+        const float lse = (m + log2f(l)) * 0.69314718055994531f;
+        if (sg.whole) args.lse[orow] = lse;
+        else args.ws_lse[static_cast<int64_t>(sg.slot) * 128 + r] = lse;
+      }
+      tc_fence_before();
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) raise_error(args.err, MLA_DEVERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// Combines the partials of every job cut into several spans; writes zeros
+// and -inf for jobs with an empty key range.  One warp per (job, head row).
+template <typename Tout>
+__global__ void __launch_bounds__(256)
+decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
+                    const float *__restrict__ ws_o,
+                    const float *__restrict__ ws_lse, Tout *out, float *lse) {
+  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
+  const int j = row >> 7, r = row & 127;
+  if (j >= J) return;
+  const int hg = j % HG;
+  if (hg * 128 + r >= H) return;
+  const int32_t *sp = plan + 4 + (J + 1);
+  const int s0 = sp[j], nseg = sp[j + 1] - s0;
+  if (nseg == 1) return;  // written directly by the decode kernel
+  const int64_t orow = static_cast<int64_t>(j / HG) * H + hg * 128 + r;
+  merge_row<float, Tout>(ws_o + (static_cast<int64_t>(s0) * 128 + r) * kLatent,
+                         static_cast<int64_t>(128) * kLatent,
+                         ws_lse + static_cast<int64_t>(s0) * 128 + r, 128, nseg,
+                         kLatent, out + orow * kLatent, lse + orow,
+                         threadIdx.x & 31);
+}
+
+struct WsLayout {
+  size_t plan_off, o_off, lse_off, total;
+  int64_t slots;
+};
+
+WsLayout ws_layout(int B, int q_len, int H, int max_seq_len, int split_tiles,
+                   int groups) {
+  const int HG = (H + 127) / 128;
+  const int64_t J = static_cast<int64_t>(B) * q_len * HG;
+  const int64_t tiles_per_job = (static_cast<int64_t>(max_seq_len) + kTile - 1) / kTile + 1;
+  const int64_t total_max = J * tiles_per_job;
+  const int64_t spans = split_tiles > 0 ? (total_max + split_tiles - 1) / split_tiles
+                                        : static_cast<int64_t>(groups);
+  WsLayout w;
+  w.slots = J + spans;
+  auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+  w.plan_off = 0;
+  w.o_off = up(plan_ints(static_cast<int>(J)) * sizeof(int32_t));
+  w.lse_off = up(w.o_off + static_cast<size_t>(w.slots) * 128 * kLatent * sizeof(float));
+  w.total = up(w.lse_off + static_cast<size_t>(w.slots) * 128 * sizeof(float));
+  return w;
+}
+
+int groups_for_device() {
+  const int sms = device_sm_count();
+  return sms >= 2 ? sms / 2 : 1;
+}
+
+bool decode_shape_ok(int B, int q_len, int H) {
+  if (B < 1 || q_len < 1 || q_len > 64 || H < 1 || H > 4096) return false;
+  const int64_t J = static_cast<int64_t>(B) * q_len * ((H + 127) / 128);
+  return J <= (1 << 22);
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int mla_decode_workspace_size(int B, int q_len, int H,
+                                         int max_seq_len, int split_tiles,
+                                         size_t *bytes) {
+  if (!bytes || !decode_shape_ok(B, q_len, H) || max_seq_len < 0 || split_tiles < 0)
+    return MLA_ERR_INVALID_ARG;
+  const int g = groups_for_device();
+  *bytes = ws_layout(B, q_len, H, max_seq_len, split_tiles, g).total;
+  return MLA_OK;
+}
+
+extern "C" int mla_decode_plan(const int32_t *seq_lens, const int32_t *kv_starts,
+                               const int32_t *kv_ends, int B, int q_len, int H,
+                               int max_blocks, int causal, int split_tiles,
+                               int n_groups, int32_t *plan, size_t plan_bytes,
+                               mla_stream_t stream) {
+  if (!decode_shape_ok(B, q_len, H) || max_blocks < 1 || split_tiles < 0 ||
+      n_groups < 0 || !seq_lens || !plan)
+    return MLA_ERR_INVALID_ARG;
+  const int HG = (H + 127) / 128;
+  const int J = B * q_len * HG;
+  if (plan_bytes < plan_ints(J) * sizeof(int32_t)) return MLA_ERR_WORKSPACE;
+  const int g = n_groups > 0 ? n_groups : groups_for_device();
+  int *err = device_error_word();
+  if (!err) return MLA_ERR_CUDA;
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, kv_starts, kv_ends, B,
+                                              q_len, HG, max_blocks, causal ? 1 : 0,
+                                              split_tiles, g, plan, err);
+  return launch_status();
+}
+
+extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
+                                const void *kv_cache, int kv_dtype,
+                                float k_scale, const int32_t *block_table,
+                                const int32_t *seq_lens,
+                                const int32_t *kv_starts,
+                                const int32_t *kv_ends, int B, int q_len,
+                                int H, int max_blocks, int num_blocks,
+                                float sm_scale, int causal, int split_tiles,
+                                void *out, int out_dtype, float *lse,
+                                void *workspace, size_t ws_bytes,
+                                mla_stream_t stream) {
+  if (!decode_shape_ok(B, q_len, H) || max_blocks < 1 || num_blocks < 1 ||
+      num_blocks >= (1 << 25) || split_tiles < 0)
+    return MLA_ERR_INVALID_ARG;
+  if (static_cast<int64_t>(max_blocks) * kPage > (1ll << 30))
+    return MLA_ERR_INVALID_ARG;
+  if (!q || !kv_cache || !block_table || !seq_lens || !out || !lse)
+    return MLA_ERR_INVALID_ARG;
+  if ((q_dtype != MLA_BF16 && q_dtype != MLA_E4M3) || q_dtype != kv_dtype)
+    return MLA_ERR_INVALID_ARG;
+  if (out_dtype != MLA_BF16 && out_dtype != MLA_F32) return MLA_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !(sm_scale < INFINITY)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out) || !aligned16(workspace))
+    return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_E4M3) return MLA_ERR_UNSUPPORTED;
+  const int g = groups_for_device();
+  const WsLayout w = ws_layout(B, q_len, H, max_blocks * kPage, split_tiles, g);
+  if (!workspace || ws_bytes < w.total) return MLA_ERR_WORKSPACE;
+  int *err = device_error_word();
+  if (!err) return MLA_ERR_CUDA;
+  const int HG = (H + 127) / 128;
+  const int J = B * q_len * HG;
+  uint8_t *ws = static_cast<uint8_t *>(workspace);
+  int32_t *plan = reinterpret_cast<int32_t *>(ws + w.plan_off);
+  float *ws_o = reinterpret_cast<float *>(ws + w.o_off);
+  float *ws_lse = reinterpret_cast<float *>(ws + w.lse_off);
+
+  plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, kv_starts, kv_ends, B,
+                                              q_len, HG, max_blocks, causal ? 1 : 0,
+                                              split_tiles, g, plan, err);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+
+  CUtensorMap tm_kv, tm_q;
+  {
+    const uint64_t dims[2] = {kDqk, static_cast<uint64_t>(num_blocks) * kPage};
+    const uint64_t strides[1] = {kDqk * 2};
+    const uint32_t box[2] = {64, kTile};
+    if (!make_tmap(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, dims,
+                   strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {kDqk, static_cast<uint64_t>(B) * q_len * H};
+    const uint64_t strides[1] = {kDqk * 2};
+    const uint32_t box[2] = {64, 128};
+    if (!make_tmap(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dims, strides,
+                   box, CU_TENSOR_MAP_SWIZZLE_128B))
+      return MLA_ERR_CUDA;
+  }
+  DecodeArgs a{};
+  a.plan = plan;
+  a.J = J;
+  a.block_table = block_table;
+  a.seq_lens = seq_lens;
+  a.q = static_cast<const __nv_bfloat16 *>(q);
+  a.q_len = q_len;
+  a.H = H;
+  a.HG = HG;
+  a.max_blocks = max_blocks;
+  a.num_blocks = num_blocks;
+  a.groups = g;
+  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.out = out;
+  a.out_dtype = out_dtype;
+  a.lse = lse;
+  a.ws_o = ws_o;
+  a.ws_lse = ws_lse;
+  a.err = err;
+  if (cudaFuncSetAttribute(decode_bf16_kernel,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  decode_bf16_kernel<<<2 * g, kThreads, kSmemBytes, stream>>>(tm_kv, tm_q, a);
+  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+
+  const int64_t rows = static_cast<int64_t>(J) * 128;
+  const dim3 mgrid(static_cast<unsigned>((rows + 7) / 8));
+  if (out_dtype == MLA_BF16)
+    decode_merge_kernel<__nv_bfloat16><<<mgrid, 256, 0, stream>>>(
+        plan, J, H, HG, ws_o, ws_lse, static_cast<__nv_bfloat16 *>(out), lse);
+  else
+    decode_merge_kernel<float><<<mgrid, 256, 0, stream>>>(
+        plan, J, H, HG, ws_o, ws_lse, static_cast<float *>(out), lse);
+  return launch_status();
+}

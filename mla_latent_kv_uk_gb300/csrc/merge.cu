@@ -1,0 +1,62 @@
+// A5/A10: LSE-rescaling merge of S partial attention states
+// (merge_attn_states).  Source: "DeepSeek MLA 在 DCP 分布式环境中的 Prefill
+// 阶段解析", §Chunked Prefill 与 LSE Merge (elementwise rescaling by the
+// partial LSEs, O(B*N*V)) and §DCP 在 Prefill 与 Decode 中的不同角色 (decode
+// combines per-rank partials by LSE weighting).
+//
+// HBM-bound: one warp per (t, h) row reads the S partial rows once with
+// 16-byte loads and writes the merged row once.
+#include <cuda_bf16.h>
+
+#include "common.cuh"
+#include "merge_row.cuh"
+
+namespace mla {
+namespace {
+
+constexpr int kWarps = 8;
+
+template <typename Tin, typename Tout>
+__global__ void __launch_bounds__(kWarps * 32)
+merge_kernel(const Tin *__restrict__ parts, const float *__restrict__ plse,
+             int S, int rows, int D, Tout *out, float *out_lse) {
+  const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);
+  if (row >= rows) return;
+  merge_row<Tin, Tout>(parts + static_cast<int64_t>(row) * D,
+                       static_cast<int64_t>(rows) * D, plse + row, rows, S, D,
+                       out + static_cast<int64_t>(row) * D,
+                       out_lse ? out_lse + row : nullptr, threadIdx.x & 31);
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
+
+extern "C" int mla_merge_states(const void *parts_out, int parts_dtype,
+                                const float *parts_lse, int S, int T, int H,
+                                int D, void *out, int out_dtype,
+                                float *out_lse, mla_stream_t stream) {
+  if (S < 1 || S > 256 || T < 0 || H < 1 || D < 8 || D > 1024 || D % 8)
+    return MLA_ERR_INVALID_ARG;
+  if ((parts_dtype != MLA_BF16 && parts_dtype != MLA_F32) ||
+      (out_dtype != MLA_BF16 && out_dtype != MLA_F32))
+    return MLA_ERR_INVALID_ARG;
+  if (T == 0) return MLA_OK;
+  if (!parts_out || !parts_lse || !out) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(parts_out) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  const int64_t rows64 = static_cast<int64_t>(T) * H;
+  if (rows64 > (1ll << 30)) return MLA_ERR_INVALID_ARG;
+  const int rows = static_cast<int>(rows64);
+  dim3 grid((rows + kWarps - 1) / kWarps);
+#define MLA_MERGE(TI, TO)                                                     \
+  merge_kernel<TI, TO><<<grid, kWarps * 32, 0, stream>>>(                     \
+      static_cast<const TI *>(parts_out), parts_lse, S, rows, D,             \
+      static_cast<TO *>(out), out_lse)
+  if (parts_dtype == MLA_BF16 && out_dtype == MLA_BF16) MLA_MERGE(__nv_bfloat16, __nv_bfloat16);
+  else if (parts_dtype == MLA_BF16) MLA_MERGE(__nv_bfloat16, float);
+  else if (out_dtype == MLA_BF16) MLA_MERGE(float, __nv_bfloat16);
+  else MLA_MERGE(float, float);
+#undef MLA_MERGE
+  return launch_status();
+}

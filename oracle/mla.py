@@ -176,7 +176,7 @@ def v_up(o_lat, w_uv):
 # A3: split-KV work plan (integer; the partition rule the kernels follow)
 # --------------------------------------------------------------------------
 
-def decode_plan(job_lo, job_hi, n_ctas, tile=32, min_tiles=4):
+def decode_plan(job_lo, job_hi, n_ctas, tile=32, min_tiles=4, forced_chunk=0):
     """Partition of every job's key tiles into contiguous per-CTA spans.
 
     DCP + FP8 KV MLA decode digest, §关键源码片段 flashmla.py (the scheduler
@@ -184,7 +184,8 @@ def decode_plan(job_lo, job_hi, n_ctas, tile=32, min_tiles=4):
     device).  Rule (this library's): a job's key range [lo, hi) covers
     absolute tiles [lo // tile, ceil(hi / tile)); jobs are concatenated in
     order into one flat tile space of ``total`` tiles; CTA group p owns flat
-    tiles [p*C, (p+1)*C) with C = max(min_tiles, ceil(total / n_ctas)).
+    tiles [p*C, (p+1)*C) with C = max(min_tiles, ceil(total / n_ctas)), or
+    C = forced_chunk when that is > 0.
     Returns dict(total, chunk, tile_prefix [J+1], seg_prefix [J+1]) where
     seg_prefix counts the spans each job is cut into (0 for empty jobs)."""
     job_lo = np.asarray(job_lo, dtype=np.int64)
@@ -193,7 +194,10 @@ def decode_plan(job_lo, job_hi, n_ctas, tile=32, min_tiles=4):
                       (job_hi + tile - 1) // tile - job_lo // tile, 0)
     tile_prefix = np.concatenate([[0], np.cumsum(ntiles)])
     total = int(tile_prefix[-1])
-    chunk = max(min_tiles, -(-total // n_ctas)) if total else min_tiles
+    if forced_chunk > 0:
+        chunk = forced_chunk
+    else:
+        chunk = max(min_tiles, -(-total // n_ctas)) if total else min_tiles
     segs = np.where(ntiles > 0,
                     (tile_prefix[1:] - 1) // chunk - tile_prefix[:-1] // chunk + 1, 0)
     seg_prefix = np.concatenate([[0], np.cumsum(segs)])

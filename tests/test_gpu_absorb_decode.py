@@ -1,0 +1,267 @@
+"""GPU parity of the absorbed decode chain against the fp64 oracle:
+absorb (+ e4m3 concat-quant, bit-exact), v_up, the split plan (bit-exact)
+and the paged decode with its on-device split merge."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import codecs, mla as O
+from tests._helpers import bits, f64, gemm_tolerance, lse_close, max_abs
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL = 1e-2      # bf16 decode output, max-abs (spec tolerance)
+LSE_TOL = 1e-3      # bf16 decode LSE, max-abs
+
+
+@pytest.fixture(scope="module")
+def m():
+    import mla_latent_kv_uk_gb300 as mod
+    return mod
+
+
+def _i32(x):
+    return torch.as_tensor(np.asarray(x, dtype=np.int32)).cuda()
+
+
+# ----------------------------------------------------------------- absorb
+@pytest.mark.parametrize("T,H", [(1, 16), (32, 128), (37, 3), (300, 8)])
+def test_absorb_bf16(m, T, H):
+    g = synth.generator(400 + T)
+    qn = synth.as_bf16(g.standard_normal((T, H, 128)))
+    qp = synth.as_bf16(g.standard_normal((T, H, 64)))
+    w = synth.as_bf16(g.standard_normal((H, 128, 512)) * 0.05)
+    q = m.mla_absorb_q(qn.cuda(), qp.cuda(), w.cuda())
+    ref = O.absorb_q(f64(qn), f64(qp), f64(w))
+    abs_sum = np.concatenate([np.einsum("thp,hpl->thl", np.abs(f64(qn)), np.abs(f64(w))),
+                              np.abs(f64(qp))], -1)
+    err = np.abs(f64(q) - ref)
+    assert np.all(err <= gemm_tolerance(ref, abs_sum)), float(err.max())
+    assert np.array_equal(bits(q)[..., 512:], bits(qp))      # q_pe copied exactly
+
+
+def test_absorb_fp32_and_e4m3_bit_exact(m):
+    """The e4m3 encoder on the GPU must give the oracle's code for the very
+    fp32 value it quantises: compare against the oracle's concat-quant of the
+    kernel's own fp32 output (same accumulation order on both launches)."""
+    g = synth.generator(410)
+    T, H = 64, 128
+    qn = synth.as_bf16(g.standard_normal((T, H, 128)))
+    qp = synth.as_bf16(g.standard_normal((T, H, 64)))
+    w = synth.as_bf16(g.standard_normal((H, 128, 512)) * 0.02)
+    q32 = m.mla_absorb_q(qn.cuda(), qp.cuda(), w.cuda(), out_dtype=torch.float32)
+    ref = O.absorb_q(f64(qn), f64(qp), f64(w))
+    abs_sum = np.concatenate([np.einsum("thp,hpl->thl", np.abs(f64(qn)), np.abs(f64(w))),
+                              np.abs(f64(qp))], -1)
+    assert np.all(np.abs(f64(q32) - ref) <= abs_sum * 2.0 ** -20 + 1e-30)
+    q_scale = float(np.float32(np.abs(f64(q32)).max() / 448.0))
+    q8 = m.mla_absorb_q(qn.cuda(), qp.cuda(), w.cuda(), out_dtype=torch.float8_e4m3fn,
+                        q_scale=q_scale)
+    want = O.concat_quant_e4m3(q32.cpu().numpy(), q_scale)
+    assert np.array_equal(bits(q8), want)
+
+
+# ------------------------------------------------------------------ v_up
+@pytest.mark.parametrize("T,H", [(1, 4), (32, 128), (256, 16), (300, 2)])
+def test_v_up(m, T, H):
+    g = synth.generator(420 + T)
+    o = synth.as_bf16(g.standard_normal((T, H, 512)))
+    w = synth.as_bf16(g.standard_normal((H, 128, 512)) * 0.02)
+    out = m.mla_v_up(o.cuda(), w.cuda())
+    ref = O.v_up(f64(o), f64(w))
+    abs_sum = np.einsum("thl,hvl->thv", np.abs(f64(o)), np.abs(f64(w)))
+    err = np.abs(f64(out) - ref)
+    assert np.all(err <= gemm_tolerance(ref, abs_sum)), float(err.max())
+
+
+# ------------------------------------------------------------------ plan
+@pytest.mark.parametrize("split_tiles,n_groups", [(0, 76), (3, 5), (0, 1), (1, 2)])
+def test_plan_matches_oracle(m, split_tiles, n_groups):
+    g = synth.generator(430)
+    B, q_len, H = 9, 2, 200
+    seq = g.integers(0, 3000, B).astype(np.int32)
+    seq[2] = 0
+    starts = g.integers(0, 50, B).astype(np.int32)
+    ends = (starts + g.integers(0, 2500, B)).astype(np.int32)
+    plan = m.mla_decode_plan(_i32(seq), B, q_len, H, 64, kv_starts=_i32(starts),
+                             kv_ends=_i32(ends), causal=True, split_tiles=split_tiles,
+                             n_groups=n_groups).cpu().numpy()
+    HG = 2
+    lo, hi = [], []
+    for b in range(B):
+        for i in range(q_len):
+            for _ in range(HG):
+                a, z = O.decode_range(int(seq[b]), q_len, i, True, starts[b], ends[b])
+                lo.append(a)
+                hi.append(z)
+    ref = O.decode_plan(lo, hi, n_groups, tile=32, min_tiles=4, forced_chunk=split_tiles)
+    J = len(lo)
+    assert plan[2] == J
+    assert plan[0] == ref["total"] and plan[1] == ref["chunk"]
+    assert np.array_equal(plan[4:4 + J + 1], ref["tile_prefix"])
+    assert np.array_equal(plan[4 + J + 1:4 + 2 * (J + 1)], ref["seg_prefix"])
+    assert np.array_equal(plan[4 + 2 * (J + 1):4 + 2 * (J + 1) + J], lo)
+    assert np.array_equal(plan[4 + 3 * (J + 1):4 + 3 * (J + 1) + J], hi)
+
+
+# ---------------------------------------------------------------- decode
+def _oracle_decode(case, kv_starts=None, kv_ends=None, causal=None):
+    q = f64(case.q) * case.q_scale
+    cache = f64(case.cache) * case.k_scale
+    return O.paged_decode(q, cache, case.block_table, case.seq_lens, case.sm_scale,
+                          causal=case.causal if causal is None else causal,
+                          kv_starts=kv_starts, kv_ends=kv_ends)
+
+
+def _run_decode(m, case, split_tiles=0, out_dtype=torch.bfloat16, kv_starts=None,
+                kv_ends=None, causal=None):
+    return m.mla_decode_paged(
+        case.q.cuda(), case.cache.cuda(), _i32(case.block_table), _i32(case.seq_lens),
+        sm_scale=case.sm_scale, q_scale=case.q_scale, k_scale=case.k_scale,
+        kv_starts=None if kv_starts is None else _i32(kv_starts),
+        kv_ends=None if kv_ends is None else _i32(kv_ends),
+        causal=case.causal if causal is None else causal, split_tiles=split_tiles,
+        out_dtype=out_dtype)
+
+
+def _check(out, lse, ref_o, ref_l, out_tol=OUT_TOL, lse_tol=LSE_TOL):
+    d_o = max_abs(f64(out), ref_o)
+    d_l, finite = lse_close(lse.cpu().numpy(), ref_l, lse_tol)
+    assert finite, "NaN in LSE"
+    assert d_o <= out_tol, f"out max-abs {d_o}"
+    assert d_l <= lse_tol, f"lse max-abs {d_l}"
+
+
+def test_decode_config1_tiny(m):
+    case = synth.config1(poison=True)
+    out, lse = _run_decode(m, case)
+    ro, rl = _oracle_decode(case)
+    _check(out, lse, ro, rl)
+    assert m.mla_get_device_error() == 0
+
+
+@pytest.mark.parametrize("split_tiles", [0, 1, 3])
+def test_decode_ragged_multi_tile(m, split_tiles):
+    case = synth.decode_case("ragged", 440, B=4, H=128, seq_lens=[1, 33, 100, 1000],
+                             poison=True)
+    out, lse = _run_decode(m, case, split_tiles=split_tiles)
+    ro, rl = _oracle_decode(case)
+    _check(out, lse, ro, rl)
+
+
+def test_decode_fp32_out_and_head_groups(m):
+    case = synth.decode_case("hg", 441, B=2, H=200, seq_lens=[77, 300], poison=True)
+    out, lse = _run_decode(m, case, out_dtype=torch.float32, split_tiles=2)
+    ro, rl = _oracle_decode(case)
+    _check(out, lse, ro, rl, out_tol=1e-3)
+
+
+def test_decode_causal_pair(m):
+    case = synth.decode_case("pair", 442, B=3, H=128, seq_lens=[2, 64, 513], q_len=2,
+                             poison=True)
+    out, lse = _run_decode(m, case, split_tiles=4)
+    ro, rl = _oracle_decode(case)
+    _check(out, lse, ro, rl)
+
+
+def test_decode_explicit_shards_then_merge(m):
+    """Config-1 shape: 2 shards per request via kv_starts/kv_ends, merged by
+    mla_merge_states, equals the unsplit decode."""
+    case = synth.config1(poison=True)
+    B = case.B
+    parts_o, parts_l = [], []
+    for s in range(2):
+        st = np.array([sh[s][0] for sh in case.shards], np.int32)
+        en = np.array([sh[s][1] for sh in case.shards], np.int32)
+        o, l = _run_decode(m, case, kv_starts=st, kv_ends=en, out_dtype=torch.float32)
+        ro, rl = _oracle_decode(case, kv_starts=st, kv_ends=en)
+        _check(o, l, ro, rl, out_tol=1e-3)
+        parts_o.append(o.reshape(B, case.H, 512))
+        parts_l.append(l.reshape(B, case.H))
+    mo, ml = m.mla_merge_states(torch.stack(parts_o), torch.stack(parts_l),
+                                out_dtype=torch.bfloat16)
+    ro, rl = _oracle_decode(case)
+    _check(mo, ml, ro.reshape(B, case.H, 512), rl.reshape(B, case.H))
+
+
+def test_decode_empty_ranges(m):
+    case = synth.decode_case("empty", 443, B=3, H=16, seq_lens=[0, 50, 50], poison=True)
+    out, lse = _run_decode(m, case, kv_starts=[0, 20, 7], kv_ends=[0, 20, 9])
+    ro, rl = _oracle_decode(case, kv_starts=[0, 20, 7], kv_ends=[0, 20, 9])
+    _check(out, lse, ro, rl)
+    assert np.all(np.isneginf(lse.cpu().numpy()[:2]))
+    assert np.all(f64(out)[:2] == 0)
+
+
+def test_decode_peaked_scores(m):
+    """Large-magnitude queries make the softmax peaked and the running max
+    jump between tiles (exercises the lazy rescale)."""
+    case = synth.decode_case("peaked", 444, B=2, H=128, seq_lens=[700, 2000], q_std=4.0,
+                             kv_std_c=0.5, kv_std_pe=0.5, poison=True)
+    out, lse = _run_decode(m, case)
+    ro, rl = _oracle_decode(case)
+    # outputs here reach |o| ~ 2; allow half a bf16 ulp on top of the budget
+    tol = OUT_TOL + 2.0 ** -8 * float(np.abs(ro).max())
+    _check(out, lse, ro, rl, out_tol=tol)
+
+
+def test_chain_absorb_decode_vup_config2_sampled(m):
+    """DeepSeek-V3 decode shape (B=32, H=128, ctx 4096) end to end; the
+    oracle checks 4 requests in full (the GPU runs all 32)."""
+    case = synth.config2()
+    q = m.mla_absorb_q(case.q_nope.cuda(), case.q_pe.cuda(), case.w_uk_t.cuda())
+    q = q.view(case.B, 1, case.H, 576)
+    out, lse = m.mla_decode_paged(q, case.cache.cuda(), _i32(case.block_table),
+                                  _i32(case.seq_lens), sm_scale=case.sm_scale)
+    y = m.mla_v_up(out.view(case.B, case.H, 512), case.w_uv.cuda())
+    pick = [0, 7, 19, 31]
+    qo = f64(q)[pick]
+    cache = f64(case.cache)
+    ro, rl = O.paged_decode(qo, cache, case.block_table[pick], case.seq_lens[pick],
+                            case.sm_scale)
+    _check(out[pick], lse[pick], ro, rl)
+    ref_y = O.v_up(f64(out)[pick][:, 0], f64(case.w_uv))
+    abs_sum = np.einsum("thl,hvl->thv", np.abs(f64(out)[pick][:, 0]), np.abs(f64(case.w_uv)))
+    assert np.all(np.abs(f64(y)[pick] - ref_y) <= gemm_tolerance(ref_y, abs_sum))
+    # end-to-end against the unrounded fp64 chain
+    q_true = O.absorb_q(f64(case.q_nope)[pick], f64(case.q_pe)[pick], f64(case.w_uk_t))
+    eo, el = O.paged_decode(q_true[:, None], cache, case.block_table[pick],
+                            case.seq_lens[pick], case.sm_scale)
+    assert max_abs(f64(out)[pick], eo) <= OUT_TOL
+    d, _ = lse_close(lse.cpu().numpy()[pick], el, LSE_TOL)
+    assert d <= 5 * LSE_TOL    # includes the bf16 rounding of the absorbed query
+
+
+def test_decode_config3_long_shards(m):
+    """ctx 131072 as 8 explicit shards (one launch, B'=8 shard rows) merged
+    on the GPU, against the unsplit oracle."""
+    case = synth.config3()
+    S = 8
+    q = case.q.cuda().expand(S, 1, case.H, 576).contiguous()
+    bt = np.repeat(case.block_table, S, axis=0)
+    seq = np.repeat(case.seq_lens, S)
+    st = np.array([a for a, _ in case.shards[0]], np.int32)
+    en = np.array([z for _, z in case.shards[0]], np.int32)
+    o, l = m.mla_decode_paged(q, case.cache.cuda(), _i32(bt), _i32(seq),
+                              sm_scale=case.sm_scale, kv_starts=_i32(st),
+                              kv_ends=_i32(en), out_dtype=torch.float32)
+    mo, ml = m.mla_merge_states(o.view(S, 1, case.H, 512), l.view(S, 1, case.H),
+                                out_dtype=torch.bfloat16)
+    ro, rl = _oracle_decode(case)
+    _check(mo, ml, ro.reshape(1, case.H, 512), rl.reshape(1, case.H))
+
+
+def test_decode_config5_sampled(m):
+    """Spec decode shape (B=128, q_len 2, lognormal ctx): all requests run,
+    12 are checked in full by the oracle."""
+    case = synth.config5_decode()
+    out, lse = _run_decode(m, case)
+    pick = [0, 1, 5, 17, 33, 50, 64, 77, 90, 101, 120, 127]
+    q = f64(case.q)[pick]
+    ro, rl = O.paged_decode(q, f64(case.cache), case.block_table[pick],
+                            case.seq_lens[pick], case.sm_scale, causal=True)
+    _check(out[pick], lse[pick], ro, rl)
