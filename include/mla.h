@@ -119,7 +119,8 @@ int mla_absorb_q(const void *q_nope, const void *q_pe, const void *w_uk_t,
  * The split of the key ranges over CTAs is planned on the device
  * (mla_decode_plan) and partial results are merged on the device; no host
  * synchronisation.  split_tiles = 0 lets the planner choose; > 0 forces
- * spans of that many 32-token tiles (testing / tuning).  workspace must
+ * spans of that many key tiles (32 tokens for bf16, 64 for e4m3; testing /
+ * tuning).  workspace must
  * hold mla_decode_workspace_size(B, q_len, H, max_blocks*64, split_tiles)
  * bytes (16-byte aligned).
  * Limits: 1 <= B, 1 <= q_len <= 64, 1 <= H <= 4096, 1 <= max_blocks,
@@ -137,10 +138,11 @@ int mla_decode_paged(const void *q, int q_dtype, float q_scale,
                      size_t ws_bytes, mla_stream_t stream);
 
 /* A3 on its own: writes the split plan that mla_decode_paged computes.
- * Jobs are (b, i, head group of 128) in that nesting order; job j covers
- * key tiles [lo/32, ceil(hi/32)); tiles of all jobs are concatenated into
- * one flat space of `total` tiles, and CTA group p owns flat tiles
- * [p*C, (p+1)*C) with C = split_tiles if > 0, else
+ * Jobs are (b, i, head group of 128) in that nesting order; with the tile
+ * size tk = 32 tokens (kv_dtype MLA_BF16) or 64 tokens (MLA_E4M3), job j
+ * covers key tiles [lo/tk, ceil(hi/tk)); tiles of all jobs are
+ * concatenated into one flat space of `total` tiles, and CTA group p owns
+ * flat tiles [p*C, (p+1)*C) with C = split_tiles if > 0, else
  * max(4, ceil(total / n_groups)).
  * plan [4 + 4*(J+1)] int32 receives: [0] total, [1] C, [2] J, [3] number
  * of spans, then tile_prefix[J+1], seg_prefix[J+1] (partial results per
@@ -148,8 +150,9 @@ int mla_decode_paged(const void *q, int q_dtype, float q_scale,
  * n_groups = 0 uses half the device's SM count. */
 int mla_decode_plan(const int32_t *seq_lens, const int32_t *kv_starts,
                     const int32_t *kv_ends, int B, int q_len, int H,
-                    int max_blocks, int causal, int split_tiles, int n_groups,
-                    int32_t *plan, size_t plan_bytes, mla_stream_t stream);
+                    int max_blocks, int causal, int kv_dtype, int split_tiles,
+                    int n_groups, int32_t *plan, size_t plan_bytes,
+                    mla_stream_t stream);
 
 /* ---------------------------------------------------------------------
  * A5/A10  LSE-rescaling merge of partial attention states

@@ -39,7 +39,7 @@ _SIGNATURES = {
     "mla_decode_workspace_size": ([_i, _i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
     "mla_decode_paged": ([_p, _i, _f, _p, _i, _f, _p, _p, _p, _p, _i, _i, _i, _i,
                           _i, _f, _i, _i, _p, _i, _p, _p, _sz, _p], _i),
-    "mla_decode_plan": ([_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _p, _sz, _p], _i),
+    "mla_decode_plan": ([_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _sz, _p], _i),
     "mla_merge_states": ([_p, _i, _p, _i, _i, _i, _i, _p, _i, _p, _p], _i),
     "mla_v_up": ([_p, _p, _i, _i, _p, _p], _i),
     "mla_gather_cache": ([_p, _i, _f, _p, _p, _p, _p, _i, _i, _i, _i, _i, _p, _p], _i),
@@ -177,14 +177,15 @@ def mla_decode_paged(q, kv_cache, block_table, seq_lens, *, sm_scale, q_scale=1.
 
 
 def mla_decode_plan(seq_lens, B, q_len, H, max_blocks, *, kv_starts=None, kv_ends=None,
-                    causal=True, split_tiles=0, n_groups=0):
+                    causal=True, kv_dtype=torch.bfloat16, split_tiles=0, n_groups=0):
     """Returns the int32 plan buffer (see include/mla.h)."""
     _req(seq_lens, "seq_lens", torch.int32, 1)
     J = B * q_len * ((H + 127) // 128)
     plan = torch.zeros(4 + 4 * (J + 1), dtype=torch.int32, device=seq_lens.device)
     _check("mla_decode_plan", lib.mla_decode_plan(
         _ptr(seq_lens), _ptr(kv_starts), _ptr(kv_ends), B, q_len, H, max_blocks,
-        int(bool(causal)), split_tiles, n_groups, _ptr(plan), plan.numel() * 4, _stream()))
+        int(bool(causal)), _DTYPE_CODE[kv_dtype], split_tiles, n_groups, _ptr(plan),
+        plan.numel() * 4, _stream()))
     return plan
 
 

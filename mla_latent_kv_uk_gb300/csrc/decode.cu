@@ -41,22 +41,53 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kTile = 32;                    // tokens per KV tile
-constexpr int kStages = 4;                   // KV ring depth
-constexpr int kBox = kTile * 128;            // one 32 x 64 bf16 box, 4 KB
-constexpr int kStageBytes = 9 * kBox;        // 576 columns, 36 KB
-constexpr int kQBox = 128 * 128;             // 128 rows x 64 bf16, 16 KB
-constexpr int kQsBoxes = 3;                  // query dims 384..575
-constexpr int kQtCols = 192;                 // query dims 0..383 in TMEM
-constexpr uint32_t kColO = 0, kColS = 256, kColQ = 320;
 constexpr int kThreads = 192;
 constexpr int kMinTiles = 4;                 // smallest auto span
 constexpr float kRescaleLog2 = 8.f;          // lazy rescale threshold
+constexpr uint32_t kColO = 0, kColS = 256;   // TMEM columns (both variants)
 
-constexpr int kSmemQ = 0;
-constexpr int kSmemKV = kQsBoxes * kQBox;                    // 48 KB
-constexpr int kSmemBar = kSmemKV + kStages * kStageBytes;    // 192 KB
-constexpr int kSmemBytes = kSmemBar + 256 + 1024;            // + align slack
+// Tile geometry of the two KV formats.  Boxes are TMA boxes of 64 latent
+// columns; a KV tile holds 9 of them (576 columns).
+template <bool FP8>
+struct Geo;
+
+template <>
+struct Geo<false> {                          // bf16 cache and query
+  static constexpr int kTile = 32;           // tokens per KV tile
+  static constexpr int kStages = 4;
+  static constexpr int kRowBytes = 128;      // 64 bf16 per box row
+  static constexpr int kBox = kTile * kRowBytes;          // 4 KB
+  static constexpr int kStageBytes = 9 * kBox;            // 36 KB
+  static constexpr int kQBox = 128 * kRowBytes;           // 16 KB
+  static constexpr int kQsBoxes = 3;         // query dims 384..575 in smem
+  static constexpr int kQtCols = 192;        // query dims 0..383 in TMEM
+  static constexpr uint32_t kColQ = 320;
+  static constexpr int kKStep = 16;          // K per MMA instruction
+  static constexpr uint32_t kSwizzle = sm100::kSwizzle128B;
+  static constexpr uint32_t kSBO = 1024;     // 8 rows x 128 B
+};
+
+template <>
+struct Geo<true> {                           // e4m3 cache and query
+  static constexpr int kTile = 64;
+  static constexpr int kStages = 4;
+  static constexpr int kRowBytes = 64;       // 64 e4m3 per box row
+  static constexpr int kBox = kTile * kRowBytes;          // 4 KB
+  static constexpr int kStageBytes = 9 * kBox;            // 36 KB
+  static constexpr int kQBox = 128 * kRowBytes;           // 8 KB
+  static constexpr int kQsBoxes = 9;         // the whole query in smem
+  static constexpr int kQtCols = 0;
+  static constexpr uint32_t kColQ = 0;
+  static constexpr int kKStep = 32;
+  static constexpr uint32_t kSwizzle = sm100::kSwizzle64B;
+  static constexpr uint32_t kSBO = 512;      // 8 rows x 64 B
+};
+
+template <bool FP8>
+constexpr int smem_bytes() {
+  return Geo<FP8>::kQsBoxes * Geo<FP8>::kQBox +
+         Geo<FP8>::kStages * Geo<FP8>::kStageBytes + 256 + 1024;
+}
 
 // ----------------------------------------------------------------- planner
 // Plan layout (int32): [0] total tiles, [1] C, [2] J, [3] spans, then
@@ -118,8 +149,8 @@ __global__ void __launch_bounds__(kPlanThreads)
 plan_kernel(const int32_t *__restrict__ seq_lens,
             const int32_t *__restrict__ kv_starts,
             const int32_t *__restrict__ kv_ends, int B, int q_len, int HG,
-            int max_blocks, int causal, int forced_chunk, int groups,
-            int32_t *plan, int *err) {
+            int max_blocks, int causal, int tile, int forced_chunk,
+            int groups, int32_t *plan, int *err) {
   __shared__ int32_t scratch[32];
   const int J = B * q_len * HG;
   int32_t *tp = plan + 4;
@@ -143,7 +174,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens,
     lo = min(max(lo, 0), hi);
     lo_a[j] = lo;
     hi_a[j] = hi;
-    tp[j] = hi > lo ? (hi + kTile - 1) / kTile - lo / kTile : 0;
+    tp[j] = hi > lo ? (hi + tile - 1) / tile - lo / tile : 0;
   }
   if (threadIdx.x == 0) { lo_a[J] = 0; hi_a[J] = 0; }
   __syncthreads();
@@ -179,14 +210,14 @@ struct Seg {
 
 struct SegWalk {
   PlanView plan;
-  int q_len, H, HG, groups;
+  int q_len, H, HG, groups, tile;
   int p, span_lo, span_hi, j;
   bool started;
 
   __device__ void init(const int32_t *pl, int J, int ql, int h, int hg,
-                       int g, int group_id) {
+                       int g, int group_id, int tile_tokens) {
     plan = PlanView{pl, J};
-    q_len = ql; H = h; HG = hg; groups = g;
+    q_len = ql; H = h; HG = hg; groups = g; tile = tile_tokens;
     p = group_id;
     started = false;
   }
@@ -225,7 +256,7 @@ struct SegWalk {
       s.hrows = min(128, H - hg * 128);
       s.lo = plan.job_lo()[j];
       s.hi = plan.job_hi()[j];
-      s.tile0 = s.lo / kTile + (u0 - a);
+      s.tile0 = s.lo / tile + (u0 - a);
       s.ntiles = u1 - u0;
       s.whole = (span_lo <= a) && (z <= span_hi);
       s.slot = plan.seg_prefix()[j] + (span_lo / C - a / C);
@@ -240,9 +271,10 @@ struct DecodeArgs {
   int J;
   const int32_t *block_table;
   const int32_t *seq_lens;
-  const __nv_bfloat16 *q;     // [B, q_len, H, 576]
+  const uint8_t *q;           // [B, q_len, H, 576] bf16 or e4m3
   int q_len, H, HG, max_blocks, num_blocks, groups;
-  float scale_log2;
+  float scale_log2;           // sm_scale * log2(e) (* q_scale * k_scale)
+  float out_scale;            // 1 (bf16) or k_scale (e4m3 values)
   void *out;
   int out_dtype;
   float *lse;
@@ -257,15 +289,45 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
   return lo | (hi << 16);
 }
 
+// Four probabilities -> four e4m3 codes in one 32-bit TMEM column (element
+// k in byte k); also returns the sum of the rounded values.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c,
+                                                float d, float &sum) {
+  const __nv_fp8x2_storage_t lo =
+      __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi =
+      __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
+  __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
+  const float2 fl = __half22float2(*reinterpret_cast<__half2 *>(&hl));
+  const float2 fh = __half22float2(*reinterpret_cast<__half2 *>(&hh));
+  sum += (fl.x + fl.y) + (fh.x + fh.y);
+  return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
+}
+
+template <bool FP8>
 __global__ void __launch_bounds__(kThreads, 1)
-decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
-                   const __grid_constant__ CUtensorMap tm_q, DecodeArgs args) {
+decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
+              const __grid_constant__ CUtensorMap tm_q, DecodeArgs args) {
+  using G = Geo<FP8>;
+  constexpr int kTile = G::kTile;
+  constexpr int kStages = G::kStages;
+  constexpr int kBox = G::kBox;
+  constexpr int kStageBytes = G::kStageBytes;
+  constexpr int kQBox = G::kQBox;
+  constexpr int kQsBoxes = G::kQsBoxes;
+  constexpr int kQsFirstCol = 576 - 64 * kQsBoxes;   // first query column in smem
+  constexpr int kQkSteps = 576 / G::kKStep;           // 36 (bf16) / 18 (e4m3)
+  constexpr int kStepsPerBox = 64 / G::kKStep;        // 4 / 2
+  constexpr int kTmemQSteps = G::kQtCols * 2 / G::kKStep;  // 24 / 0
+  constexpr int kPvSteps = kTile / G::kKStep;         // 2 / 2
+
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sm_q = smem + kSmemQ;
-  uint8_t *sm_kv = smem + kSmemKV;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kSmemBar);
+  uint8_t *sm_q = smem;
+  uint8_t *sm_kv = smem + kQsBoxes * kQBox;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_kv + kStages * kStageBytes);
   uint64_t *kv_full = bars;                 // [kStages]
   uint64_t *kv_empty = bars + kStages;      // [kStages]
   uint64_t *s_full = bars + 2 * kStages;    // [2]
@@ -309,7 +371,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
   const uint32_t tmem = *tmem_slot;
 
   SegWalk walk;
-  walk.init(args.plan, args.J, args.q_len, args.H, args.HG, args.groups, group);
+  walk.init(args.plan, args.J, args.q_len, args.H, args.HG, args.groups, group, kTile);
   Seg sg;
 
   if (warp == 0) {
@@ -324,13 +386,14 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
         const int s = kc % kStages;
         if (kc >= kStages && !mbar_wait(&kv_empty[s], ((kc / kStages) - 1) & 1, abort_flag))
           return false;
-        const int blk = __ldg(bt + tile / 2);
+        const int tok = tile * kTile;
+        const int blk = __ldg(bt + tok / kPage);
         int row;
         if (blk < 0 || blk >= args.num_blocks) {
           raise_error(args.err, MLA_DEVERR_BLOCK_ID);
           row = args.num_blocks * kPage;  // out of range: TMA fills zeros
         } else {
-          row = blk * kPage + (tile & 1) * kTile;
+          row = blk * kPage + tok % kPage;
         }
         uint8_t *dst = sm_kv + s * kStageBytes;
         mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
@@ -349,7 +412,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
         if (nseg > 0 && !(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
         mbar_arrive_expect_tx(q_full, kQsBoxes * kQBox);
         for (int k = 0; k < kQsBoxes; ++k)
-          tma_load_2d(sm_q + k * kQBox, &tm_q, q_full, 384 + 64 * k, sg.row0);
+          tma_load_2d(sm_q + k * kQBox, &tm_q, q_full, kQsFirstCol + 64 * k, sg.row0);
         ++nseg;
         for (int t = pre; ok && t < sg.ntiles; ++t) ok = load_tile(bt, sg.tile0 + t);
       }
@@ -363,25 +426,29 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
   } else if (warp == 1) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      const uint32_t idesc_qk = idesc_bf16(128, kTile, false, false);
-      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      const uint32_t idesc_qk = FP8 ? idesc_e4m3(128, kTile, false, false)
+                                    : idesc_bf16(128, kTile, false, false);
+      const uint32_t idesc_pv = FP8 ? idesc_e4m3(128, 256, false, true)
+                                    : idesc_bf16(128, 256, false, true);
       const uint32_t q_base = smem_u32(sm_q);
       int kc = 0, uc = 0, nseg = 0;
       bool ok = true;
       auto issue_qk = [&](int kcx, int ucx) {
         const uint32_t stage = smem_u32(sm_kv + (kcx % kStages) * kStageBytes);
-        const uint32_t d = tmem + kColS + 32 * (ucx & 1);
+        const uint32_t d = tmem + kColS + kTile * (ucx & 1);
 #pragma unroll 4
-        for (int k = 0; k < 36; ++k) {
-          const uint64_t bdesc =
-              sdesc(stage + (k >> 2) * kBox + (k & 3) * 32, 16, 1024, kSwizzle128B);
-          if (k < 24) {
-            mma_f16_ts(d, tmem + kColQ + 8 * k, bdesc, idesc_qk, k > 0);
+        for (int k = 0; k < kQkSteps; ++k) {
+          const uint32_t off = (k / kStepsPerBox) * kBox + (k % kStepsPerBox) * 32;
+          const uint64_t bdesc = sdesc(stage + off, 16, G::kSBO, G::kSwizzle);
+          if (k < kTmemQSteps) {
+            mma_f16_ts(d, tmem + G::kColQ + 8 * k, bdesc, idesc_qk, k > 0);
           } else {
-            const int kq = k - 24;
-            const uint64_t adesc = sdesc(q_base + (kq >> 2) * kQBox + (kq & 3) * 32,
-                                         16, 1024, kSwizzle128B);
-            mma_f16_ss(d, adesc, bdesc, idesc_qk, 1);
+            const int kq = k - kTmemQSteps;
+            const uint64_t adesc =
+                sdesc(q_base + (kq / kStepsPerBox) * kQBox + (kq % kStepsPerBox) * 32, 16,
+                      G::kSBO, G::kSwizzle);
+            if (FP8) mma_f8_ss(d, adesc, bdesc, idesc_qk, k > 0);
+            else mma_f16_ss(d, adesc, bdesc, idesc_qk, k > 0);
           }
         }
         mma_commit(&s_full[ucx & 1]);
@@ -408,11 +475,14 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
           tc_fence_after();
           const uint32_t stage = smem_u32(sm_kv + (kc % kStages) * kStageBytes);
 #pragma unroll
-          for (int kk = 0; kk < 2; ++kk) {
-            const uint64_t bdesc = sdesc(stage + (4 * half) * kBox + kk * 2048,
-                                         kBox, 1024, kSwizzle128B);
-            mma_f16_ts(tmem + kColO, tmem + kColS + 32 * (uc & 1) + 8 * kk, bdesc,
-                       idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kPvSteps; ++kk) {
+            // value half: boxes 4*half..4*half+3 (64 latent columns each),
+            // MN-major: N-blocks one box apart (LBO), 8-token groups SBO apart
+            const uint64_t bdesc = sdesc(stage + (4 * half) * kBox + kk * 2048, kBox,
+                                         G::kSBO, G::kSwizzle);
+            const uint32_t a = tmem + kColS + kTile * (uc & 1) + 8 * kk;
+            if (FP8) mma_f8_ts(tmem + kColO, a, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+            else mma_f16_ts(tmem + kColO, a, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&kv_empty[kc % kStages]);
           mma_commit(pv_done);
@@ -431,28 +501,27 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
     const int r = quarter * 32 + lane;  // head row within the group
     const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
     const int tid = threadIdx.x - 64;   // 0..127
-    int uc = 0, npv = 0, nseg = 0;
+    int uc = 0, npv = 0;
     bool ok = true;
     while (ok && walk.next(sg)) {
-      // query dims 0..383 of row r -> TMEM columns [kColQ, kColQ + 192)
-      {
+      if (G::kQtCols > 0) {
+        // query dims 0..383 of row r -> TMEM columns [kColQ, kColQ + 192)
         const uint4 *src = reinterpret_cast<const uint4 *>(
-            args.q + static_cast<int64_t>(sg.row0 + r) * kDqk);
+            args.q + static_cast<int64_t>(sg.row0 + r) * kDqk * 2);
         const bool valid = r < sg.hrows;
 #pragma unroll 1
-        for (int c = 0; c < kQtCols / 32; ++c) {
+        for (int c = 0; c < G::kQtCols / 32; ++c) {
           uint32_t w[32];
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
             uint4 v = valid ? __ldg(src + c * 8 + k) : make_uint4(0, 0, 0, 0);
             w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
           }
-          tmem_st_x32(lane_base + kColQ + 32 * c, w);
+          tmem_st_x32(lane_base + G::kColQ + 32 * c, w);
         }
         tc_fence_before();
-        mbar_arrive(q_tmem);
       }
-      ++nseg;
+      mbar_arrive(q_tmem);
       float m = -INFINITY, l = 0.f;
       const int len = __ldg(args.seq_lens + sg.b);
       for (int t = 0; t < sg.ntiles; ++t, ++uc) {
@@ -460,17 +529,20 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
         ok = mbar_wait(&s_full[sb], (uc >> 1) & 1, abort_flag);
         if (!ok) break;
         tc_fence_after();
-        uint32_t sr[32];
-        tmem_ld_x32(lane_base + kColS + 32 * sb, sr);
         const int pos0 = (sg.tile0 + t) * kTile;
-        float x[32];
+        float x[kTile];
         float tmax = -INFINITY;
 #pragma unroll
-        for (int jj = 0; jj < 32; ++jj) {
-          const int pos = pos0 + jj;
-          const bool valid = pos >= sg.lo && pos < sg.hi;
-          x[jj] = valid ? __uint_as_float(sr[jj]) * args.scale_log2 : -INFINITY;
-          tmax = fmaxf(tmax, x[jj]);
+        for (int c = 0; c < kTile; c += 32) {
+          uint32_t sr[32];
+          tmem_ld_x32(lane_base + kColS + kTile * sb + c, sr);
+#pragma unroll
+          for (int jj = 0; jj < 32; ++jj) {
+            const int pos = pos0 + c + jj;
+            const bool valid = pos >= sg.lo && pos < sg.hi;
+            x[c + jj] = valid ? __uint_as_float(sr[jj]) * args.scale_log2 : -INFINITY;
+            tmax = fmaxf(tmax, x[c + jj]);
+          }
         }
         if (t > 0) {
           ok = mbar_wait(pv_done, npv & 1, abort_flag);
@@ -498,15 +570,20 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
         }
         uint32_t pk[16];
         float psum = 0.f;
+        if (FP8) {
 #pragma unroll
-        for (int jj = 0; jj < 16; ++jj) {
-          const float p0 = exp2f(x[2 * jj] - m);
-          const float p1 = exp2f(x[2 * jj + 1] - m);
-          pk[jj] = pack_bf16(p0, p1);
-          psum += __uint_as_float(pk[jj] << 16) + __uint_as_float(pk[jj] & 0xFFFF0000u);
+          for (int k = 0; k < 16; ++k)
+            pk[k] = pack_e4m3x4(exp2f(x[4 * k] - m), exp2f(x[4 * k + 1] - m),
+                                exp2f(x[4 * k + 2] - m), exp2f(x[4 * k + 3] - m), psum);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            pk[k] = pack_bf16(exp2f(x[2 * k] - m), exp2f(x[2 * k + 1] - m));
+            psum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+          }
         }
         l += psum;
-        tmem_st_x16(lane_base + kColS + 32 * sb, pk);
+        tmem_st_x16(lane_base + kColS + kTile * sb, pk);
         if (pos0 + kTile > len) {
           // Cache rows past seq_len may hold anything (even NaN bits): zero
           // this CTA's value columns of those rows so that P = 0 really
@@ -514,11 +591,13 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
           // uc % kStages (the producer fills stages in the same order).
           const int first = max(0, len - pos0);
           const int nrows = kTile - first;
+          constexpr int kChunks = G::kRowBytes / 16;
           uint8_t *vbase = sm_kv + (uc % kStages) * kStageBytes + (4 * half) * kBox;
-          for (int idx = tid; idx < nrows * 32; idx += 128) {
-            const int box = idx / (nrows * 8);
-            const int rem = idx - box * nrows * 8;
-            reinterpret_cast<uint4 *>(vbase + box * kBox + (first + rem / 8) * 128)[rem % 8] =
+          for (int idx = tid; idx < nrows * 4 * kChunks; idx += 128) {
+            const int box = idx / (nrows * kChunks);
+            const int rem = idx - box * nrows * kChunks;
+            reinterpret_cast<uint4 *>(vbase + box * kBox +
+                                      (first + rem / kChunks) * G::kRowBytes)[rem % kChunks] =
                 make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
@@ -532,7 +611,7 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
       if (!ok) break;
       tc_fence_after();
       // ---- epilogue: O / l for this CTA's 256 latent columns
-      const float inv = 1.f / l;
+      const float inv = args.out_scale / l;
       const bool row_ok = r < sg.hrows;
       const int64_t orow = static_cast<int64_t>(sg.out_row0 + r);
 #pragma unroll 1
@@ -544,26 +623,20 @@ decode_bf16_kernel(const __grid_constant__ CUtensorMap tm_kv,
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
         const int col = 256 * half + c;
-        if (sg.whole) {
-          if (args.out_dtype == MLA_BF16) {
-            uint4 *dst = reinterpret_cast<uint4 *>(
-                static_cast<__nv_bfloat16 *>(args.out) + orow * kLatent + col);
+        if (sg.whole && args.out_dtype == MLA_BF16) {
+          uint4 *dst = reinterpret_cast<uint4 *>(
+              static_cast<__nv_bfloat16 *>(args.out) + orow * kLatent + col);
 #pragma unroll
-            for (int k = 0; k < 4; ++k)
-              dst[k] = make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]),
-                                  pack_bf16(v[8 * k + 2], v[8 * k + 3]),
-                                  pack_bf16(v[8 * k + 4], v[8 * k + 5]),
-                                  pack_bf16(v[8 * k + 6], v[8 * k + 7]));
-          } else {
-            float4 *dst = reinterpret_cast<float4 *>(
-                static_cast<float *>(args.out) + orow * kLatent + col);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-          }
+          for (int k = 0; k < 4; ++k)
+            dst[k] = make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]),
+                                pack_bf16(v[8 * k + 2], v[8 * k + 3]),
+                                pack_bf16(v[8 * k + 4], v[8 * k + 5]),
+                                pack_bf16(v[8 * k + 6], v[8 * k + 7]));
         } else {
-          float4 *dst = reinterpret_cast<float4 *>(
-              args.ws_o + (static_cast<int64_t>(sg.slot) * 128 + r) * kLatent + col);
+          float *base = sg.whole
+                            ? static_cast<float *>(args.out) + orow * kLatent + col
+                            : args.ws_o + (static_cast<int64_t>(sg.slot) * 128 + r) * kLatent + col;
+          float4 *dst = reinterpret_cast<float4 *>(base);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
             dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
@@ -617,7 +690,8 @@ WsLayout ws_layout(int B, int q_len, int H, int max_seq_len, int split_tiles,
                    int groups) {
   const int HG = (H + 127) / 128;
   const int64_t J = static_cast<int64_t>(B) * q_len * HG;
-  const int64_t tiles_per_job = (static_cast<int64_t>(max_seq_len) + kTile - 1) / kTile + 1;
+  // bound with the smaller (bf16) tile: at least as many tiles as e4m3's
+  const int64_t tiles_per_job = (static_cast<int64_t>(max_seq_len) + 31) / 32 + 1;
   const int64_t total_max = J * tiles_per_job;
   const int64_t spans = split_tiles > 0 ? (total_max + split_tiles - 1) / split_tiles
                                         : static_cast<int64_t>(groups);
@@ -659,23 +733,58 @@ extern "C" int mla_decode_workspace_size(int B, int q_len, int H,
 
 extern "C" int mla_decode_plan(const int32_t *seq_lens, const int32_t *kv_starts,
                                const int32_t *kv_ends, int B, int q_len, int H,
-                               int max_blocks, int causal, int split_tiles,
-                               int n_groups, int32_t *plan, size_t plan_bytes,
-                               mla_stream_t stream) {
+                               int max_blocks, int causal, int kv_dtype,
+                               int split_tiles, int n_groups, int32_t *plan,
+                               size_t plan_bytes, mla_stream_t stream) {
   if (!decode_shape_ok(B, q_len, H) || max_blocks < 1 || split_tiles < 0 ||
       n_groups < 0 || !seq_lens || !plan)
     return MLA_ERR_INVALID_ARG;
+  if (kv_dtype != MLA_BF16 && kv_dtype != MLA_E4M3) return MLA_ERR_INVALID_ARG;
   const int HG = (H + 127) / 128;
   const int J = B * q_len * HG;
   if (plan_bytes < plan_ints(J) * sizeof(int32_t)) return MLA_ERR_WORKSPACE;
   const int g = n_groups > 0 ? n_groups : groups_for_device();
   int *err = device_error_word();
   if (!err) return MLA_ERR_CUDA;
+  const int tile = kv_dtype == MLA_E4M3 ? Geo<true>::kTile : Geo<false>::kTile;
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, kv_starts, kv_ends, B,
                                               q_len, HG, max_blocks, causal ? 1 : 0,
-                                              split_tiles, g, plan, err);
+                                              tile, split_tiles, g, plan, err);
   return launch_status();
 }
+
+namespace {
+
+template <bool FP8>
+int launch_decode(const void *q, const void *kv_cache, int B, int q_len, int H,
+                  int num_blocks, DecodeArgs a, mla_stream_t stream) {
+  using G = Geo<FP8>;
+  const CUtensorMapDataType dt =
+      FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw = FP8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const uint64_t row_bytes = static_cast<uint64_t>(kDqk) * (FP8 ? 1 : 2);
+  CUtensorMap tm_kv, tm_q;
+  {
+    const uint64_t dims[2] = {kDqk, static_cast<uint64_t>(num_blocks) * kPage};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {64, static_cast<uint32_t>(G::kTile)};
+    if (!make_tmap(&tm_kv, dt, 2, kv_cache, dims, strides, box, sw)) return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[2] = {kDqk, static_cast<uint64_t>(B) * q_len * H};
+    const uint64_t strides[1] = {row_bytes};
+    const uint32_t box[2] = {64, 128};
+    if (!make_tmap(&tm_q, dt, 2, q, dims, strides, box, sw)) return MLA_ERR_CUDA;
+  }
+  constexpr int smem = smem_bytes<FP8>();
+  if (cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           smem) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  decode_kernel<FP8><<<2 * a.groups, kThreads, smem, stream>>>(tm_kv, tm_q, a);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+}  // namespace
 
 extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
                                 const void *kv_cache, int kv_dtype,
@@ -699,9 +808,12 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
     return MLA_ERR_INVALID_ARG;
   if (out_dtype != MLA_BF16 && out_dtype != MLA_F32) return MLA_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !(sm_scale < INFINITY)) return MLA_ERR_INVALID_ARG;
+  const bool fp8 = kv_dtype == MLA_E4M3;
+  if (fp8 && (!(q_scale > 0.f) || !(q_scale < INFINITY) || !(k_scale > 0.f) ||
+              !(k_scale < INFINITY)))
+    return MLA_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out) || !aligned16(workspace))
     return MLA_ERR_INVALID_ARG;
-  if (kv_dtype == MLA_E4M3) return MLA_ERR_UNSUPPORTED;
   const int g = groups_for_device();
   const WsLayout w = ws_layout(B, q_len, H, max_blocks * kPage, split_tiles, g);
   if (!workspace || ws_bytes < w.total) return MLA_ERR_WORKSPACE;
@@ -714,53 +826,35 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   float *ws_o = reinterpret_cast<float *>(ws + w.o_off);
   float *ws_lse = reinterpret_cast<float *>(ws + w.lse_off);
 
+  const int tile = fp8 ? Geo<true>::kTile : Geo<false>::kTile;
   plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, kv_starts, kv_ends, B,
                                               q_len, HG, max_blocks, causal ? 1 : 0,
-                                              split_tiles, g, plan, err);
+                                              tile, split_tiles, g, plan, err);
   if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
 
-  CUtensorMap tm_kv, tm_q;
-  {
-    const uint64_t dims[2] = {kDqk, static_cast<uint64_t>(num_blocks) * kPage};
-    const uint64_t strides[1] = {kDqk * 2};
-    const uint32_t box[2] = {64, kTile};
-    if (!make_tmap(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, dims,
-                   strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return MLA_ERR_CUDA;
-  }
-  {
-    const uint64_t dims[2] = {kDqk, static_cast<uint64_t>(B) * q_len * H};
-    const uint64_t strides[1] = {kDqk * 2};
-    const uint32_t box[2] = {64, 128};
-    if (!make_tmap(&tm_q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, dims, strides,
-                   box, CU_TENSOR_MAP_SWIZZLE_128B))
-      return MLA_ERR_CUDA;
-  }
   DecodeArgs a{};
   a.plan = plan;
   a.J = J;
   a.block_table = block_table;
   a.seq_lens = seq_lens;
-  a.q = static_cast<const __nv_bfloat16 *>(q);
+  a.q = static_cast<const uint8_t *>(q);
   a.q_len = q_len;
   a.H = H;
   a.HG = HG;
   a.max_blocks = max_blocks;
   a.num_blocks = num_blocks;
   a.groups = g;
-  a.scale_log2 = sm_scale * 1.4426950408889634f;
+  a.scale_log2 = sm_scale * 1.4426950408889634f * (fp8 ? q_scale * k_scale : 1.f);
+  a.out_scale = fp8 ? k_scale : 1.f;
   a.out = out;
   a.out_dtype = out_dtype;
   a.lse = lse;
   a.ws_o = ws_o;
   a.ws_lse = ws_lse;
   a.err = err;
-  if (cudaFuncSetAttribute(decode_bf16_kernel,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess)
-    return MLA_ERR_CUDA;
-  decode_bf16_kernel<<<2 * g, kThreads, kSmemBytes, stream>>>(tm_kv, tm_q, a);
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  const int st = fp8 ? launch_decode<true>(q, kv_cache, B, q_len, H, num_blocks, a, stream)
+                     : launch_decode<false>(q, kv_cache, B, q_len, H, num_blocks, a, stream);
+  if (st != MLA_OK) return st;
 
   const int64_t rows = static_cast<int64_t>(J) * 128;
   const dim3 mgrid(static_cast<unsigned>((rows + 7) / 8));

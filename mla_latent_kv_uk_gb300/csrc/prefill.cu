@@ -1,23 +1,330 @@
-// A8 kv_b_proj expansion and A9 prefill attention (chunked-prefill context
-// step).  Source: "DeepSeek MLA 在 DCP 分布式环境中的 Prefill 阶段解析",
-// §MLA Prefill vs Decode and §Chunked Prefill 与 LSE Merge.
-#include "common.cuh"
+// A9: prefill multi-head attention with LSE (run_prefill_new_tokens is the
+// causal case, run_prefill_context_chunk the non-causal one).
+//
+// Source: "DeepSeek MLA 在 DCP 分布式环境中的 Prefill 阶段解析", §Chunked
+// Prefill 与 LSE Merge (new tokens attend causally to themselves and return
+// the softmax LSE; context chunks are attended without a mask; the two are
+// merged by LSE) and §MLA Prefill vs Decode (prefill uses expanded heads:
+// QK width 128 + 64 = 192, V width 128).
+//
+// One CTA per (128 query rows, head, request).  Per 128-key tile:
+//   S = Q K^T   tcgen05 M=128 N=128 K=192 (12 MMAs) into a TMEM buffer,
+//   P = exp2(S*scale*log2e - m) as bf16 written back over S in TMEM,
+//   O += P V    tcgen05 with A = P from TMEM, B = V (MN-major) from smem.
+// TMEM: S/P double buffer [0,256), O [256,384).  TMA fills a 2-stage ring
+// of K (48 KB) + V (32 KB) tiles.  Warp 0 = TMA, warp 1 = MMA, warps 2..5 =
+// softmax + epilogue (one query row per thread); lazy O rescaling.
+#include <cuda_bf16.h>
+#include <math.h>
 
-extern "C" int mla_expand_kv(const void *kv_rows, const void *w_kvb, int N,
-                             int H, void *k_out, void *v_out,
-                             mla_stream_t stream) {
-  (void)kv_rows; (void)w_kvb; (void)N; (void)H; (void)k_out; (void)v_out;
-  (void)stream;
-  return MLA_ERR_UNSUPPORTED;
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace mla {
+namespace {
+
+using namespace sm100;
+
+constexpr int kBM = 128, kBN = 128;
+constexpr int kDq = 192, kDv = 128;
+constexpr int kBox = 128 * 128;                  // 128 rows x 64 bf16
+constexpr int kQBytes = 3 * kBox;                // 48 KB
+constexpr int kKBytes = 3 * kBox;                // 48 KB
+constexpr int kVBytes = 2 * kBox;                // 32 KB
+constexpr int kStages = 2;
+constexpr int kStageBytes = kKBytes + kVBytes;
+constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + 256 + 1024;
+constexpr int kThreads = 192;
+constexpr uint32_t kColS = 0, kColO = 256;
+constexpr float kRescaleLog2 = 8.f;
+
+struct PrefillArgs {
+  const int32_t *cu_q, *cu_k;
+  int H, causal;
+  float scale_log2;
+  __nv_bfloat16 *out;
+  float *lse;
+};
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
 }
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
+               const __grid_constant__ CUtensorMap tm_k,
+               const __grid_constant__ CUtensorMap tm_v, PrefillArgs args,
+               int *err) {
+  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int q0 = __ldg(args.cu_q + b), nq = __ldg(args.cu_q + b + 1) - q0;
+  const int k0 = __ldg(args.cu_k + b), nk = __ldg(args.cu_k + b + 1) - k0;
+  if (qt * kBM >= nq) return;  // uniform across the CTA: nothing allocated yet
+  const int rows = min(kBM, nq - qt * kBM);
+  // keys visible to the last row of this tile
+  int key_end = nk;
+  if (args.causal) key_end = min(nk, qt * kBM + rows - 1 + nk - nq + 1);
+  key_end = max(key_end, 0);
+  const int ntiles = (key_end + kBN - 1) / kBN;
+
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sm_q = smem;
+  uint8_t *sm_kv = smem + kQBytes;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_kv + kStages * kStageBytes);
+  uint64_t *kv_full = bars, *kv_empty = bars + kStages;
+  uint64_t *s_full = bars + 2 * kStages, *p_full = s_full + 2;
+  uint64_t *pv_done = p_full + 2, *q_full = pv_done + 1, *drain = q_full + 1;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const int warp = warp_id(), lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+    }
+    mbar_init(pv_done, 1);
+    mbar_init(q_full, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    bool ok = true;
+    int t = 0;
+    if (ntiles > 0) {
+      mbar_arrive_expect_tx(q_full, kQBytes);
+      for (int d = 0; d < 3; ++d)
+        tma_load_3d(sm_q + d * kBox, &tm_q, q_full, 64 * d, h, q0 + qt * kBM);
+    }
+    for (; t < ntiles; ++t) {
+      const int s = t % kStages;
+      if (t >= kStages && !(ok = mbar_wait(&kv_empty[s], ((t / kStages) - 1) & 1, abort_flag)))
+        break;
+      uint8_t *dst = sm_kv + s * kStageBytes;
+      mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+      const int row = k0 + t * kBN;
+      for (int d = 0; d < 3; ++d) tma_load_3d(dst + d * kBox, &tm_k, &kv_full[s], 64 * d, h, row);
+      for (int d = 0; d < 2; ++d)
+        tma_load_3d(dst + kKBytes + d * kBox, &tm_v, &kv_full[s], 64 * d, h, row);
+    }
+    if (*abort_flag) {
+      volatile int no_abort = 0;
+      for (int k = max(0, t - kStages); k < t; ++k)
+        mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &no_abort);
+      if (ntiles > 0) mbar_wait(q_full, 0, &no_abort);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc_qk = idesc_bf16(128, kBN, false, false);
+    const uint32_t idesc_pv = idesc_bf16(128, kDv, false, true);
+    const uint32_t qa = smem_u32(sm_q);
+    bool ok = ntiles == 0 || mbar_wait(q_full, 0, abort_flag);
+    auto issue_qk = [&](int t) {
+      const uint32_t kb = smem_u32(sm_kv + (t % kStages) * kStageBytes);
+      const uint32_t d = tmem + kColS + 128 * (t & 1);
+#pragma unroll
+      for (int k = 0; k < kDq / 16; ++k)
+        mma_f16_ss(d, sdesc(qa + (k >> 2) * kBox + (k & 3) * 32, 16, 1024, kSwizzle128B),
+                   sdesc(kb + (k >> 2) * kBox + (k & 3) * 32, 16, 1024, kSwizzle128B),
+                   idesc_qk, k > 0);
+      mma_commit(&s_full[t & 1]);
+    };
+    if (ok && ntiles > 0) {
+      ok = mbar_wait(&kv_full[0], 0, abort_flag);
+      if (ok) {
+        tc_fence_after();
+        issue_qk(0);
+      }
+    }
+    for (int t = 0; ok && t < ntiles; ++t) {
+      if (t + 1 < ntiles) {
+        if (!(ok = mbar_wait(&kv_full[(t + 1) % kStages], ((t + 1) / kStages) & 1, abort_flag)))
+          break;
+        tc_fence_after();
+        issue_qk(t + 1);
+      }
+      if (!(ok = mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      const uint32_t vb = smem_u32(sm_kv + (t % kStages) * kStageBytes + kKBytes);
+#pragma unroll
+      for (int kk = 0; kk < kBN / 16; ++kk)
+        mma_f16_ts(tmem + kColO, tmem + kColS + 128 * (t & 1) + 8 * kk,
+                   sdesc(vb + kk * 2048, kBox, 1024, kSwizzle128B), idesc_pv,
+                   (t > 0 || kk > 0) ? 1u : 0u);
+      mma_commit(&kv_empty[t % kStages]);
+      mma_commit(pv_done);
+    }
+    if (!ok) {
+      mma_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort);
+    }
+  } else if (warp >= 2) {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
+    const int i = qt * kBM + r;                      // query index in request
+    const int lim = args.causal ? min(nk, i + nk - nq + 1) : nk;
+    float m = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < ntiles; ++t) {
+      const int sb = t & 1;
+      if (!(ok = mbar_wait(&s_full[sb], (t >> 1) & 1, abort_flag))) break;
+      tc_fence_after();
+      float x[kBN];
+      float tmax = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kBN; c += 32) {
+        uint32_t v[32];
+        tmem_ld_x32(lane_base + kColS + 128 * sb + c, v);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          const int j = t * kBN + c + k;
+          x[c + k] = j < lim ? __uint_as_float(v[k]) * args.scale_log2 : -INFINITY;
+          tmax = fmaxf(tmax, x[c + k]);
+        }
+      }
+      if (t > 0) {
+        if (!(ok = mbar_wait(pv_done, (t - 1) & 1, abort_flag))) break;
+        tc_fence_after();
+        const float m_new = fmaxf(m, tmax);
+        const bool need = m_new > m + kRescaleLog2 || (m == -INFINITY && m_new > -INFINITY);
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? (m == -INFINITY ? 0.f : exp2f(m - m_new)) : 1.f;
+#pragma unroll 1
+          for (int c = 0; c < kDv; c += 32) {
+            uint32_t o[32];
+            tmem_ld_x32(lane_base + kColO + c, o);
+#pragma unroll
+            for (int k = 0; k < 32; ++k)
+              o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+            tmem_st_x32(lane_base + kColO + c, o);
+          }
+          l *= alpha;
+          if (need) m = m_new;
+        }
+      } else {
+        m = tmax;
+      }
+      const float ms = m == -INFINITY ? 0.f : m;
+      float psum = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN; c += 64) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          pk[k] = pack2(exp2f(x[c + 2 * k] - ms), exp2f(x[c + 2 * k + 1] - ms));
+          psum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+        }
+        tmem_st_x32(lane_base + kColS + 128 * sb + c / 2, pk);
+      }
+      l += psum;
+      tc_fence_before();
+      mbar_arrive(&p_full[sb]);
+    }
+    if (ok && ntiles > 0) ok = mbar_wait(pv_done, (ntiles - 1) & 1, abort_flag);
+    tc_fence_after();
+    if (ok) {
+      const bool row_ok = r < rows;
+      const int64_t orow = static_cast<int64_t>(q0 + i) * args.H + h;
+      const bool empty = !(l > 0.f);
+      const float inv = empty ? 0.f : 1.f / l;
+#pragma unroll 1
+      for (int c = 0; c < kDv; c += 32) {
+        uint32_t o[32];
+        if (ntiles > 0) tmem_ld_x32(lane_base + kColO + c, o);
+        if (!row_ok) continue;
+        uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv + c);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          float v[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            v[e] = (ntiles > 0 && !empty) ? __uint_as_float(o[8 * k + e]) * inv : 0.f;
+          dst[k] = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]),
+                              pack2(v[6], v[7]));
+        }
+      }
+      if (row_ok)
+        args.lse[orow] = empty ? -INFINITY : (m + log2f(l)) * 0.69314718055994531f;
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) raise_error(err, MLA_DEVERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+}  // namespace
+}  // namespace mla
+
+using namespace mla;
 
 extern "C" int mla_prefill_attn(const void *q, const void *k, const void *v,
                                 const int32_t *cu_q, const int32_t *cu_k,
                                 int B, int Tq, int Nk, int H, int max_q_len,
                                 int causal, float sm_scale, void *out,
                                 float *lse, mla_stream_t stream) {
-  (void)q; (void)k; (void)v; (void)cu_q; (void)cu_k; (void)B; (void)Tq;
-  (void)Nk; (void)H; (void)max_q_len; (void)causal; (void)sm_scale;
-  (void)out; (void)lse; (void)stream;
-  return MLA_ERR_UNSUPPORTED;
+  if (B < 1 || Tq < 0 || Nk < 0 || H < 1 || H > 65535 || max_q_len < 0 || B > 65535)
+    return MLA_ERR_INVALID_ARG;
+  if (!(sm_scale > 0.f) || !(sm_scale < INFINITY)) return MLA_ERR_INVALID_ARG;
+  if (Tq == 0 || max_q_len == 0) return MLA_OK;
+  if (!q || !k || !v || !cu_q || !cu_k || !out || !lse) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return MLA_ERR_INVALID_ARG;
+  int *err = device_error_word();
+  if (!err) return MLA_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  const uint32_t box[3] = {64, 1, 128};
+  {
+    const uint64_t dims[3] = {kDq, static_cast<uint64_t>(H), static_cast<uint64_t>(Tq)};
+    const uint64_t strides[2] = {kDq * 2, static_cast<uint64_t>(H) * kDq * 2};
+    if (!make_tmap(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return MLA_ERR_CUDA;
+  }
+  const uint64_t nk_rows = Nk > 0 ? static_cast<uint64_t>(Nk) : 1;
+  {
+    const uint64_t dims[3] = {kDq, static_cast<uint64_t>(H), nk_rows};
+    const uint64_t strides[2] = {kDq * 2, static_cast<uint64_t>(H) * kDq * 2};
+    if (!make_tmap(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, k, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t dims[3] = {kDv, static_cast<uint64_t>(H), nk_rows};
+    const uint64_t strides[2] = {kDv * 2, static_cast<uint64_t>(H) * kDv * 2};
+    if (!make_tmap(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, v, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_128B))
+      return MLA_ERR_CUDA;
+  }
+  PrefillArgs a{cu_q, cu_k, H, causal ? 1 : 0, sm_scale * 1.4426950408889634f,
+                static_cast<__nv_bfloat16 *>(out), lse};
+  if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  dim3 grid((max_q_len + kBM - 1) / kBM, H, B);
+  prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, a, err);
+  return launch_status();
 }

@@ -79,8 +79,10 @@ def test_v_up(m, T, H):
 
 
 # ------------------------------------------------------------------ plan
-@pytest.mark.parametrize("split_tiles,n_groups", [(0, 76), (3, 5), (0, 1), (1, 2)])
-def test_plan_matches_oracle(m, split_tiles, n_groups):
+@pytest.mark.parametrize("split_tiles,n_groups,fp8", [(0, 76, False), (3, 5, False),
+                                                     (0, 1, False), (1, 2, False),
+                                                     (0, 76, True), (2, 3, True)])
+def test_plan_matches_oracle(m, split_tiles, n_groups, fp8):
     g = synth.generator(430)
     B, q_len, H = 9, 2, 200
     seq = g.integers(0, 3000, B).astype(np.int32)
@@ -89,7 +91,9 @@ def test_plan_matches_oracle(m, split_tiles, n_groups):
     ends = (starts + g.integers(0, 2500, B)).astype(np.int32)
     plan = m.mla_decode_plan(_i32(seq), B, q_len, H, 64, kv_starts=_i32(starts),
                              kv_ends=_i32(ends), causal=True, split_tiles=split_tiles,
-                             n_groups=n_groups).cpu().numpy()
+                             n_groups=n_groups,
+                             kv_dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16
+                             ).cpu().numpy()
     HG = 2
     lo, hi = [], []
     for b in range(B):
@@ -98,7 +102,8 @@ def test_plan_matches_oracle(m, split_tiles, n_groups):
                 a, z = O.decode_range(int(seq[b]), q_len, i, True, starts[b], ends[b])
                 lo.append(a)
                 hi.append(z)
-    ref = O.decode_plan(lo, hi, n_groups, tile=32, min_tiles=4, forced_chunk=split_tiles)
+    ref = O.decode_plan(lo, hi, n_groups, tile=64 if fp8 else 32, min_tiles=4,
+                        forced_chunk=split_tiles)
     J = len(lo)
     assert plan[2] == J
     assert plan[0] == ref["total"] and plan[1] == ref["chunk"]
@@ -265,3 +270,37 @@ def test_decode_config5_sampled(m):
     ro, rl = O.paged_decode(q, f64(case.cache), case.block_table[pick],
                             case.seq_lens[pick], case.sm_scale, causal=True)
     _check(out[pick], lse[pick], ro, rl)
+
+
+# ------------------------------------------------------------- fp8 decode
+FP8_OUT_TOL, FP8_LSE_TOL = 5e-2, 1e-2
+
+
+@pytest.mark.parametrize("split_tiles", [0, 2])
+def test_decode_fp8_ragged(m, split_tiles):
+    case = synth.decode_case("fp8_small", 450, B=3, H=128, seq_lens=[5, 100, 700],
+                             kv_dtype="e4m3", q_dtype="e4m3", poison=True)
+    out, lse = _run_decode(m, case, split_tiles=split_tiles)
+    ro, rl = _oracle_decode(case)
+    _check(out, lse, ro, rl, out_tol=FP8_OUT_TOL, lse_tol=FP8_LSE_TOL)
+    assert m.mla_get_device_error() == 0
+
+
+def test_decode_fp8_causal_pair_head_groups(m):
+    case = synth.decode_case("fp8_pair", 451, B=2, H=144, seq_lens=[70, 1000], q_len=2,
+                             kv_dtype="e4m3", q_dtype="e4m3", poison=True)
+    out, lse = _run_decode(m, case, out_dtype=torch.float32)
+    ro, rl = _oracle_decode(case)
+    _check(out, lse, ro, rl, out_tol=FP8_OUT_TOL, lse_tol=FP8_LSE_TOL)
+
+
+def test_decode_config4_fp8_sampled(m):
+    """FP8 KV shape (B=64, ctx U[1024,16384], e4m3 cache and query with
+    per-tensor scales): all requests run, 6 are checked in full."""
+    case = synth.config4()
+    out, lse = _run_decode(m, case)
+    pick = [0, 9, 21, 40, 52, 63]
+    q = f64(case.q)[pick] * case.q_scale
+    ro, rl = O.paged_decode(q, f64(case.cache) * case.k_scale, case.block_table[pick],
+                            case.seq_lens[pick], case.sm_scale)
+    _check(out[pick], lse[pick], ro, rl, out_tol=FP8_OUT_TOL, lse_tol=FP8_LSE_TOL)

@@ -1,0 +1,128 @@
+"""GPU parity of the chunked-prefill context step: kv_b_proj expansion,
+prefill attention (causal / non-causal, with LSE) and the full config-5
+chain (sharded gather + reorg -> expand -> context attention, new-token
+causal attention -> merge) against the fp64 oracle."""
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import mla as O
+from tests._helpers import f64, gemm_tolerance, lse_close, max_abs
+
+pytestmark = pytest.mark.gpu
+
+OUT_TOL, LSE_TOL = 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module")
+def m():
+    import mla_latent_kv_uk_gb300 as mod
+    return mod
+
+
+def _i32(x):
+    return torch.as_tensor(np.asarray(x, dtype=np.int32)).cuda()
+
+
+@pytest.mark.parametrize("N,H", [(1, 1), (300, 3), (128, 16)])
+def test_expand(m, N, H):
+    g = synth.generator(500 + N)
+    kv = synth.as_bf16(g.standard_normal((N, 576)))
+    w = synth.as_bf16(g.standard_normal((H * 256, 512)) * 0.02)
+    K, V = m.mla_expand_kv(kv.cuda(), w.cuda(), H)
+    rk, rv = O.expand_kv(f64(kv), f64(w), H)
+    absk = np.einsum("nl,hcl->nhc", np.abs(f64(kv)[:, :512]),
+                     np.abs(f64(w)).reshape(H, 256, 512))
+    assert np.all(np.abs(f64(K)[..., :128] - rk[..., :128])
+                  <= gemm_tolerance(rk[..., :128], absk[..., :128]))
+    assert np.array_equal(f64(K)[..., 128:], rk[..., 128:])
+    assert np.all(np.abs(f64(V) - rv) <= gemm_tolerance(rv, absk[..., 128:]))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_prefill_attention_small(m, causal):
+    g = synth.generator(510 + causal)
+    H = 4
+    nq = np.array([100, 200, 1, 129])
+    nk = np.array([300, 200, 1, 129]) if causal else np.array([300, 150, 7, 500])
+    cu_q = np.concatenate([[0], np.cumsum(nq)]).astype(np.int32)
+    cu_k = np.concatenate([[0], np.cumsum(nk)]).astype(np.int32)
+    q = synth.as_bf16(g.standard_normal((cu_q[-1], H, 192)))
+    k = synth.as_bf16(g.standard_normal((cu_k[-1], H, 192)))
+    v = synth.as_bf16(g.standard_normal((cu_k[-1], H, 128)))
+    scale = 1 / np.sqrt(192)
+    out, lse = m.mla_prefill_attn(q.cuda(), k.cuda(), v.cuda(), _i32(cu_q), _i32(cu_k),
+                                  int(nq.max()), causal=causal, sm_scale=scale)
+    ro, rl = O.prefill_attention(f64(q), f64(k), f64(v), cu_q, cu_k, causal, scale)
+    assert max_abs(f64(out), ro) <= OUT_TOL
+    d, fin = lse_close(lse.cpu().numpy(), rl, LSE_TOL)
+    assert fin and d <= LSE_TOL
+
+
+def test_prefill_no_visible_keys(m):
+    """Causal with fewer keys than queries: the first rows see no key and
+    return out = 0, lse = -inf."""
+    H = 2
+    cu_q = np.array([0, 5], np.int32)
+    cu_k = np.array([0, 2], np.int32)
+    g = synth.generator(520)
+    q = synth.as_bf16(g.standard_normal((5, H, 192)))
+    k = synth.as_bf16(g.standard_normal((2, H, 192)))
+    v = synth.as_bf16(g.standard_normal((2, H, 128)))
+    out, lse = m.mla_prefill_attn(q.cuda(), k.cuda(), v.cuda(), _i32(cu_q), _i32(cu_k), 5,
+                                  causal=True, sm_scale=0.1)
+    ro, rl = O.prefill_attention(f64(q), f64(k), f64(v), cu_q, cu_k, True, 0.1)
+    assert np.all(np.isneginf(lse.cpu().numpy()[:3])) and np.all(np.isneginf(rl[:3]))
+    assert max_abs(f64(out), ro) <= OUT_TOL
+
+
+def test_chunked_prefill_config5_sampled(m):
+    """Config 5 context step: 4 requests x 8192 context rows on 4 interleaved
+    shards, 512 new tokens each; gather+reorg -> expand -> non-causal context
+    attention; new tokens expand -> causal attention; LSE merge.  The oracle
+    checks 2 heads x 16 query rows per request (it expands only those heads)."""
+    case = synth.config5_prefill()
+    W, I, H = case.W, case.interleave, case.H
+    ctx, new = case.ctx_lens, case.new_lens
+    smb = max(s[1].shape[1] for s in case.shards)
+    tables = []
+    for _, sbt, _ in case.shards:
+        t = np.full((case.B, smb), -1, np.int32)
+        t[:, :sbt.shape[1]] = sbt
+        tables.append(_i32(t))
+    cu_c = np.concatenate([[0], np.cumsum(ctx)]).astype(np.int32)
+    cu_q = np.concatenate([[0], np.cumsum(new)]).astype(np.int32)
+    rows, _ = m.mla_gather_cache_reorg([s[0].cuda() for s in case.shards], tables,
+                                       _i32(cu_c), int(cu_c[-1]), interleave=I)
+    w = case.w_kvb.cuda()
+    kc, vc = m.mla_expand_kv(rows, w, H)
+    kn, vn = m.mla_expand_kv(case.new_kv.cuda(), w, H)
+    q = case.q.cuda()
+    oc, lc = m.mla_prefill_attn(q, kc, vc, _i32(cu_q), _i32(cu_c), int(new.max()),
+                                causal=False, sm_scale=case.sm_scale)
+    on, ln = m.mla_prefill_attn(q, kn, vn, _i32(cu_q), _i32(cu_q), int(new.max()),
+                                causal=True, sm_scale=case.sm_scale)
+    Tq = int(cu_q[-1])
+    out, lse = m.mla_merge_states(torch.stack([oc, on]), torch.stack([lc, ln]),
+                                  out_dtype=torch.bfloat16)
+    assert m.mla_get_device_error() == 0
+    # oracle on sampled heads / rows
+    heads = [0, 77]
+    g = synth.generator(530)
+    q_rows = np.concatenate([cu_q[b] + np.sort(g.choice(new[b], 16, replace=False))
+                             for b in range(case.B)])
+    ctx_rows = O.gather_cache(f64(case.cache), case.block_table, cu_c)
+    Kc, Vc = O.expand_kv(ctx_rows, f64(case.w_kvb), H, heads=heads)
+    Kn, Vn = O.expand_kv(f64(case.new_kv), f64(case.w_kvb), H, heads=heads)
+    qs = f64(case.q)[:, heads]
+    ro, rl, merges = O.chunked_prefill(qs, Kn, Vn, Kc, Vc, cu_q, cu_c, case.sm_scale,
+                                       n_chunks=1, q_rows=q_rows)
+    assert merges == 1
+    got_o = f64(out)[q_rows][:, heads]
+    got_l = lse.cpu().numpy()[q_rows][:, heads]
+    assert max_abs(got_o, ro[q_rows]) <= OUT_TOL
+    d, fin = lse_close(got_l, rl[q_rows], LSE_TOL)
+    assert fin and d <= 2 * LSE_TOL
+    assert Tq == 2048
