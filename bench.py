@@ -110,6 +110,21 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
+def max_over_ranks(values, world, device):
+    """Per-rank timings -> the maximum over all ranks (replicas run
+    independently; this reduction is measurement plumbing, not data path)."""
+    if world <= 1:
+        return list(values)
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(units_per_rank, world, ms_max):
+    """Aggregate throughput: units all ranks processed / slowest rank's time."""
+    return units_per_rank * world / (ms_max * 1e-3)
+
+
 def make_inputs(device):
     import synth
     case = synth.config2(B=B, ctx=CTX)
@@ -203,26 +218,21 @@ def run_ours(args, rank, world, device):
     e2e_tot, _ = timed(e2e_step, args.steps, has_dec=False)
     err = m.mla_get_device_error()
 
-    ms = statistics.mean(tot)
-    ms_e2e = statistics.mean(e2e_tot)
-    ms_dec = statistics.mean(dec) if dec else float("nan")
-    if world > 1:
-        t = torch.tensor([ms, ms_e2e, ms_dec], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms, ms_e2e, ms_dec = t.tolist()
+    ms, ms_e2e, ms_dec = max_over_ranks(
+        [statistics.mean(tot), statistics.mean(e2e_tot),
+         statistics.mean(dec) if dec else float("nan")], world, device)
     bytes_, flops, kv_tokens = algorithmic_counts(case.seq_lens, B, H)
     hbm, bf16, src = peaks()
-    tokens = B * world
     achieved = bytes_ / (ms_dec * 1e-3) / 1e9
     res = {
-        "metric": METRIC, "value": tokens / (ms * 1e-3), "unit": "tokens/s",
+        "metric": METRIC, "value": whole_job_rate(B, world, ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded, random-init weights)",
         "config": {"workload": WORKLOAD, "batch": B, "heads": H, "ctx": CTX,
                    "kv_tokens": kv_tokens, "page": 64, "l2": "flushed (512 MiB write) before every step",
                    "parallelism": "replicas" if world > 1 else "single"},
-        "e2e": {"value": tokens / (ms_e2e * 1e-3), "unit": "tokens/s",
+        "e2e": {"value": whole_job_rate(B, world, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
                      "frac": achieved / hbm, "traffic": None,

@@ -436,7 +436,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
       auto issue_qk = [&](int kcx, int ucx) {
         const uint32_t stage = smem_u32(sm_kv + (kcx % kStages) * kStageBytes);
         const uint32_t d = tmem + kColS + kTile * (ucx & 1);
-#pragma unroll 4
+#pragma unroll
         for (int k = 0; k < kQkSteps; ++k) {
           const uint32_t off = (k / kStepsPerBox) * kBox + (k % kStepsPerBox) * 32;
           const uint64_t bdesc = sdesc(stage + off, 16, G::kSBO, G::kSwizzle);
@@ -503,12 +503,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
     const int tid = threadIdx.x - 64;   // 0..127
     int uc = 0, npv = 0;
     bool ok = true;
-    while (ok && walk.next(sg)) {
+    // Query dims 0..383 of row r of segment `seg` -> TMEM [kColQ, kColQ+192).
+    // Done for the next segment as soon as the previous one's MMAs are over
+    // (before its epilogue), so the next QK MMAs overlap that epilogue.
+    auto load_q_tmem = [&](const Seg &seg) {
       if (G::kQtCols > 0) {
-        // query dims 0..383 of row r -> TMEM columns [kColQ, kColQ + 192)
         const uint4 *src = reinterpret_cast<const uint4 *>(
-            args.q + static_cast<int64_t>(sg.row0 + r) * kDqk * 2);
-        const bool valid = r < sg.hrows;
+            args.q + static_cast<int64_t>(seg.row0 + r) * kDqk * 2);
+        const bool valid = r < seg.hrows;
 #pragma unroll 1
         for (int c = 0; c < G::kQtCols / 32; ++c) {
           uint32_t w[32];
@@ -522,6 +524,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         tc_fence_before();
       }
       mbar_arrive(q_tmem);
+    };
+    bool have = walk.next(sg);
+    if (have) load_q_tmem(sg);
+    while (ok && have) {
       float m = -INFINITY, l = 0.f;
       const int len = __ldg(args.seq_lens + sg.b);
       for (int t = 0; t < sg.ntiles; ++t, ++uc) {
@@ -610,10 +616,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
       ++npv;
       if (!ok) break;
       tc_fence_after();
+      // every MMA of this segment is done: stage the next segment's query
+      const Seg cur = sg;
+      have = walk.next(sg);
+      if (have) load_q_tmem(sg);
       // ---- epilogue: O / l for this CTA's 256 latent columns
       const float inv = args.out_scale / l;
-      const bool row_ok = r < sg.hrows;
-      const int64_t orow = static_cast<int64_t>(sg.out_row0 + r);
+      const bool row_ok = r < cur.hrows;
+      const int64_t orow = static_cast<int64_t>(cur.out_row0 + r);
 #pragma unroll 1
       for (int c = 0; c < 256; c += 32) {
         uint32_t o[32];
@@ -623,7 +633,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
         const int col = 256 * half + c;
-        if (sg.whole && args.out_dtype == MLA_BF16) {
+        if (cur.whole && args.out_dtype == MLA_BF16) {
           uint4 *dst = reinterpret_cast<uint4 *>(
               static_cast<__nv_bfloat16 *>(args.out) + orow * kLatent + col);
 #pragma unroll
@@ -633,9 +643,9 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
                                 pack_bf16(v[8 * k + 4], v[8 * k + 5]),
                                 pack_bf16(v[8 * k + 6], v[8 * k + 7]));
         } else {
-          float *base = sg.whole
+          float *base = cur.whole
                             ? static_cast<float *>(args.out) + orow * kLatent + col
-                            : args.ws_o + (static_cast<int64_t>(sg.slot) * 128 + r) * kLatent + col;
+                            : args.ws_o + (static_cast<int64_t>(cur.slot) * 128 + r) * kLatent + col;
           float4 *dst = reinterpret_cast<float4 *>(base);
 #pragma unroll
           for (int k = 0; k < 8; ++k)
@@ -644,8 +654,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
       }
       if (row_ok && half == 0) {
         const float lse = (m + log2f(l)) * 0.69314718055994531f;
-        if (sg.whole) args.lse[orow] = lse;
-        else args.ws_lse[static_cast<int64_t>(sg.slot) * 128 + r] = lse;
+        if (cur.whole) args.lse[orow] = lse;
+        else args.ws_lse[static_cast<int64_t>(cur.slot) * 128 + r] = lse;
       }
       tc_fence_before();
     }
