@@ -1,0 +1,125 @@
+"""Pin strength: plant one plausible mistake at a time in the oracle (on the
+CPU, by monkeypatching) and check that at least one pin test fails.  The
+oracle itself is never modified."""
+
+import numpy as np
+import pytest
+
+import oracle.mla as O
+from tests import test_oracle_decode as D
+from tests import test_oracle_gather_prefill as G
+
+
+def _fails(*pins):
+    for pin in pins:
+        try:
+            pin()
+        except AssertionError:
+            return True
+    return False
+
+
+def test_causal_off_by_one(monkeypatch):
+    orig = O.decode_range
+
+    def bad(seq_len, q_len, i, causal, kv_start=None, kv_end=None):
+        lo, hi = orig(seq_len, q_len, i, causal, kv_start, kv_end)
+        return (lo, max(lo, hi - 1)) if causal else (lo, hi)
+    monkeypatch.setattr(O, "decode_range", bad)
+    assert _fails(D.test_paged_addressing_matches_contiguous,
+                  D.test_causal_pair_reduces_to_single_token_decode)
+
+
+def test_lse_without_max_term(monkeypatch):
+    def bad(q_rows, keys, values, sm_scale):
+        H = q_rows.shape[0]
+        if keys.shape[0] == 0:
+            return np.zeros((H, values.shape[1])), np.full(H, -np.inf)
+        s = sm_scale * (q_rows @ keys.T)
+        m = s.max(axis=1, keepdims=True)
+        e = np.exp(s - m)
+        z = e.sum(axis=1, keepdims=True)
+        return (e / z) @ values, np.log(z)[:, 0]          # forgot + m
+    monkeypatch.setattr(O, "attend", bad)
+    assert _fails(D.test_attend_brute_force, D.test_attend_golden_two_keys)
+
+
+def test_scale_missing_in_scores(monkeypatch):
+    orig = O.attend
+    monkeypatch.setattr(O, "attend", lambda q, k, v, s: orig(q, k, v, 1.0))
+    assert _fails(D.test_attend_brute_force, D.test_attend_golden_two_keys)
+
+
+def test_merge_weight_sign(monkeypatch):
+    def bad(parts_out, parts_lse):
+        parts_lse = np.asarray(parts_lse, float)
+        m = parts_lse.max(axis=0)
+        w = np.exp(m[None] - parts_lse)                     # inverted
+        z = w.sum(axis=0)
+        return (np.asarray(parts_out) * w[..., None]).sum(0) / z[..., None], m + np.log(z)
+    monkeypatch.setattr(O, "merge_states", bad)
+    assert _fails(lambda: D.test_merge_of_shards_equals_unsplit("contiguous"))
+
+
+def test_absorb_wrong_contraction(monkeypatch):
+    def bad(q_nope, q_pe, w_uk_t):
+        # contracts over the wrong weight axis pattern (per-head transpose)
+        ql = np.einsum("thp,hpl->thl", q_nope[..., ::-1], w_uk_t)
+        return np.concatenate([ql, q_pe], axis=-1)
+    monkeypatch.setattr(O, "absorb_q", bad)
+    assert _fails(D.test_absorb_brute_force, D.test_absorbed_mqa_equals_expanded_mha)
+
+
+def test_v_up_transposed_weight(monkeypatch):
+    monkeypatch.setattr(O, "v_up", lambda o, w: np.einsum("thl,hvl->thv", o, w[:, ::-1]))
+    assert _fails(D.test_v_up_brute_force, D.test_absorbed_mqa_equals_expanded_mha)
+
+
+def test_expand_swapped_halves(monkeypatch):
+    orig = O.expand_kv
+
+    def bad(kv_rows, w_kvb, H, heads=None):
+        w = np.asarray(w_kvb).reshape(H, 256, 512)[:, ::-1].reshape(H * 256, 512)
+        return orig(kv_rows, w, H, heads)
+    monkeypatch.setattr(O, "expand_kv", bad)
+    assert _fails(G.test_expand_brute_force, D.test_absorbed_mqa_equals_expanded_mha)
+
+
+def test_reorg_ignores_interleave(monkeypatch):
+    monkeypatch.setattr(O, "shard_local_index",
+                        lambda t, W, I: (np.asarray(t) % W, np.asarray(t) // W))
+    assert _fails(lambda: G.test_reorg_inverts_interleaved_sharding(4, 3),
+                  G.test_shard_local_index_is_a_bijection)
+
+
+def test_gather_ignores_seq_starts(monkeypatch):
+    orig = O.gather_cache
+    monkeypatch.setattr(O, "gather_cache",
+                        lambda c, bt, cu, seq_starts=None: orig(c, bt, cu, None))
+    assert _fails(G.test_gather_seq_starts_equals_slice_of_full_gather)
+
+
+def test_plan_segment_count_off_by_one(monkeypatch):
+    orig = O.decode_plan
+
+    def bad(*a, **k):
+        r = orig(*a, **k)
+        sp = r["seg_prefix"].copy()
+        sp[1:] += np.arange(1, len(sp))       # one extra segment per job
+        r["seg_prefix"] = sp
+        return r
+    monkeypatch.setattr(O, "decode_plan", bad)
+    assert _fails(lambda: G.test_plan_covers_each_job_exactly_once(7))
+
+
+def test_prefill_causal_shift(monkeypatch):
+    orig = O.prefill_attention
+
+    def bad(q, k, v, cu_q, cu_k, causal, sm_scale, q_rows=None):
+        if causal:   # aligns the mask top-left instead of bottom-right
+            cu_k2 = np.asarray(cu_k).copy()
+            return orig(q, k, v, cu_q, cu_k2, True, sm_scale * 1.01, q_rows)
+        return orig(q, k, v, cu_q, cu_k, causal, sm_scale, q_rows)
+    monkeypatch.setattr(O, "prefill_attention", bad)
+    assert _fails(G.test_prefill_causal_brute_force,
+                  lambda: G.test_chunked_prefill_equals_full_attention(2))
