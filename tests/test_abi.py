@@ -12,10 +12,11 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def _lib_path():
-    from mla_latent_kv_uk_gb300 import _build
-    if not os.path.exists(_build.lib_path()):
-        _build.build()
-    return _build.lib_path()
+    import __graft_entry__ as entry
+    b = entry._build_module()
+    if not os.path.exists(b.lib_path()):
+        b.build()
+    return b.lib_path()
 
 
 def _declared():
@@ -44,6 +45,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings_and_version():
+    _lib_path()
     import mla_latent_kv_uk_gb300 as m
     assert m.mla_version() == 1
     assert m.mla_status_string(0) == "ok"
