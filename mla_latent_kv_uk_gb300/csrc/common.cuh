@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "mla.h"
 
 namespace mla {
@@ -32,6 +34,25 @@ bool make_tmap(CUtensorMap *map, CUtensorMapDataType dtype, int rank,
                const void *base, const uint64_t *dims,
                const uint64_t *strides_bytes, const uint32_t *box,
                CUtensorMapSwizzle swizzle);
+
+// Launches `kern` on `stream` with programmatic stream serialization, so it
+// may be scheduled while the previous grid in the stream is still running;
+// the kernel must call griddepcontrol.wait before reading that grid's output.
+template <typename... Params, typename... Args>
+inline cudaError_t launch_pdl(void (*kern)(Params...), dim3 grid, dim3 block,
+                              size_t smem, cudaStream_t stream, Args &&...args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
 
 inline int launch_status() {
   return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;

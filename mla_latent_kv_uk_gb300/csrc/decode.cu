@@ -152,6 +152,9 @@ plan_kernel(const int32_t *__restrict__ seq_lens,
             int max_blocks, int causal, int tile, int forced_chunk,
             int groups, int32_t *plan, int *err) {
   __shared__ int32_t scratch[32];
+  // the decode grid may be scheduled now; it waits for this grid to finish
+  // before it reads the plan
+  sm100::grid_dep_launch();
   const int J = B * q_len * HG;
   int32_t *tp = plan + 4;
   int32_t *sp = tp + (J + 1);
@@ -272,6 +275,7 @@ struct DecodeArgs {
   const int32_t *block_table;
   const int32_t *seq_lens;
   const uint8_t *q;           // [B, q_len, H, 576] bf16 or e4m3
+  const uint8_t *kv;          // [num_blocks, 64, 576] (L2 prefetch source)
   int q_len, H, HG, max_blocks, num_blocks, groups;
   float scale_log2;           // sm_scale * log2(e) (* q_scale * k_scale)
   float out_scale;            // 1 (bf16) or k_scale (e4m3 values)
@@ -290,18 +294,13 @@ __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
 }
 
 // Four probabilities -> four e4m3 codes in one 32-bit TMEM column (element
-// k in byte k); also returns the sum of the rounded values.
+// k in byte k).
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c,
-                                                float d, float &sum) {
+                                                float d) {
   const __nv_fp8x2_storage_t lo =
       __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
   const __nv_fp8x2_storage_t hi =
       __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
-  __half2_raw hl = __nv_cvt_fp8x2_to_halfraw2(lo, __NV_E4M3);
-  __half2_raw hh = __nv_cvt_fp8x2_to_halfraw2(hi, __NV_E4M3);
-  const float2 fl = __half22float2(*reinterpret_cast<__half2 *>(&hl));
-  const float2 fh = __half22float2(*reinterpret_cast<__half2 *>(&hh));
-  sum += (fl.x + fl.y) + (fh.x + fh.y);
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
@@ -369,59 +368,100 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // the prologue above overlaps the plan kernel; the plan is read below
+  grid_dep_wait();
+  grid_dep_launch();
 
   SegWalk walk;
   walk.init(args.plan, args.J, args.q_len, args.H, args.HG, args.groups, group, kTile);
   Seg sg;
 
   if (warp == 0) {
+    // -------------------------------------------------- TMA producer
+    // The whole warp walks the work; lane 0 issues barrier and TMA
+    // operations.  Block-table entries are fetched 32 pages at a time (one
+    // per lane) and broadcast with shuffles, so no tile waits on a global
+    // load; CTA half 0 also prefetches tiles kPrefetch ahead into L2, where
+    // the TMA loads of both CTAs of the pair find them.
     if (lane == 0) {
-      // ------------------------------------------------ TMA producer
       prefetch_tmap(&tm_kv);
       prefetch_tmap(&tm_q);
-      int kc = 0, nseg = 0;
-      bool ok = true;
-      // Loads KV tile `tile` of request row `bt` into ring slot kc % kStages.
-      auto load_tile = [&](const int32_t *bt, int tile) -> bool {
+    }
+    constexpr int kPrefetch = 16;
+    constexpr int kRowBytes = FP8 ? kDqk : kDqk * 2;
+    int kc = 0, nseg = 0;
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      const int32_t *bt = args.block_table + static_cast<int64_t>(sg.b) * args.max_blocks;
+      int page_base = -(1 << 30), my_blk = -1;
+      auto blk_of = [&](int tile) -> int {  // warp-collective
+        const int page = tile * kTile / kPage;
+        if (page < page_base || page >= page_base + 32) {
+          page_base = page;
+          my_blk = page + lane < args.max_blocks ? __ldg(bt + page + lane) : -1;
+        }
+        return __shfl_sync(0xffffffffu, my_blk, page - page_base);
+      };
+      auto row_of = [&](int tile, int blk) -> int {
+        return blk * kPage + (tile * kTile) % kPage;
+      };
+      int pf = 0;  // tiles of this segment prefetched so far
+      auto prefetch_upto = [&](int t_end) {
+        t_end = min(t_end, sg.ntiles);
+        while (pf < t_end) {
+          const int tile = sg.tile0 + pf;
+          const int blk = blk_of(tile);
+          if (half == 0 && lane == 0 && blk >= 0 && blk < args.num_blocks)
+            prefetch_l2(args.kv + static_cast<int64_t>(row_of(tile, blk)) * kRowBytes,
+                        kStageBytes);
+          ++pf;
+        }
+      };
+      // Loads KV tile `tile` into ring slot kc % kStages.
+      auto load_tile = [&](int tile) -> bool {
         const int s = kc % kStages;
         if (kc >= kStages && !mbar_wait(&kv_empty[s], ((kc / kStages) - 1) & 1, abort_flag))
           return false;
-        const int tok = tile * kTile;
-        const int blk = __ldg(bt + tok / kPage);
-        int row;
-        if (blk < 0 || blk >= args.num_blocks) {
-          raise_error(args.err, MLA_DEVERR_BLOCK_ID);
-          row = args.num_blocks * kPage;  // out of range: TMA fills zeros
-        } else {
-          row = blk * kPage + tok % kPage;
+        const int blk = blk_of(tile);
+        if (lane == 0) {
+          int row;
+          if (blk < 0 || blk >= args.num_blocks) {
+            raise_error(args.err, MLA_DEVERR_BLOCK_ID);
+            row = args.num_blocks * kPage;  // out of range: TMA fills zeros
+          } else {
+            row = row_of(tile, blk);
+          }
+          uint8_t *dst = sm_kv + s * kStageBytes;
+          mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+          for (int d = 0; d < 9; ++d)
+            tma_load_2d(dst + d * kBox, &tm_kv, &kv_full[s], 64 * d, row);
         }
-        uint8_t *dst = sm_kv + s * kStageBytes;
-        mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
-        for (int d = 0; d < 9; ++d)
-          tma_load_2d(dst + d * kBox, &tm_kv, &kv_full[s], 64 * d, row);
         ++kc;
         return true;
       };
-      while (ok && walk.next(sg)) {
-        const int32_t *bt = args.block_table + static_cast<int64_t>(sg.b) * args.max_blocks;
-        // The first ring-full of this segment's tiles only needs free ring
-        // slots; the query slot frees when the previous segment's MMAs end.
-        const int pre = min(sg.ntiles, kStages);
-        for (int t = 0; ok && t < pre; ++t) ok = load_tile(bt, sg.tile0 + t);
-        if (!ok) break;
-        if (nseg > 0 && !(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
+      prefetch_upto(kPrefetch);
+      // The first ring-full of this segment's tiles only needs free ring
+      // slots; the query slot frees when the previous segment's MMAs end.
+      const int pre = min(sg.ntiles, kStages);
+      for (int t = 0; ok && t < pre; ++t) ok = load_tile(sg.tile0 + t);
+      if (!ok) break;
+      if (nseg > 0 && !(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
+      if (lane == 0) {
         mbar_arrive_expect_tx(q_full, kQsBoxes * kQBox);
         for (int k = 0; k < kQsBoxes; ++k)
           tma_load_2d(sm_q + k * kQBox, &tm_q, q_full, kQsFirstCol + 64 * k, sg.row0);
-        ++nseg;
-        for (int t = pre; ok && t < sg.ntiles; ++t) ok = load_tile(bt, sg.tile0 + t);
       }
-      if (*abort_flag) {
-        volatile int no_abort = 0;
-        for (int k = max(0, kc - kStages); k < kc; ++k)
-          mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &no_abort);
-        if (nseg > 0) mbar_wait(q_full, (nseg - 1) & 1, &no_abort);
+      ++nseg;
+      for (int t = pre; ok && t < sg.ntiles; ++t) {
+        prefetch_upto(t + kPrefetch);
+        ok = load_tile(sg.tile0 + t);
       }
+    }
+    if (*abort_flag && lane == 0) {
+      volatile int no_abort = 0;
+      for (int k = max(0, kc - kStages); k < kc; ++k)
+        mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &no_abort);
+      if (nseg > 0) mbar_wait(q_full, (nseg - 1) & 1, &no_abort);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -511,15 +551,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         const uint4 *src = reinterpret_cast<const uint4 *>(
             args.q + static_cast<int64_t>(seg.row0 + r) * kDqk * 2);
         const bool valid = r < seg.hrows;
+        // 3 batches of 16 independent 16-byte loads (two TMEM stores each)
 #pragma unroll 1
-        for (int c = 0; c < G::kQtCols / 32; ++c) {
-          uint32_t w[32];
+        for (int c = 0; c < G::kQtCols / 64; ++c) {
+          uint32_t w[64];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            uint4 v = valid ? __ldg(src + c * 8 + k) : make_uint4(0, 0, 0, 0);
+          for (int k = 0; k < 16; ++k) {
+            uint4 v = valid ? __ldg(src + c * 16 + k) : make_uint4(0, 0, 0, 0);
             w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
           }
-          tmem_st_x32(lane_base + G::kColQ + 32 * c, w);
+          tmem_st_x32(lane_base + G::kColQ + 64 * c, w);
+          tmem_st_x32(lane_base + G::kColQ + 64 * c + 32, w + 32);
         }
         tc_fence_before();
       }
@@ -574,21 +616,24 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         } else {
           m = tmax;
         }
-        uint32_t pk[16];
+        // The row sum uses the unrounded fp32 probabilities: the LSE then
+        // carries no rounding of P, and O / l differs from the exact
+        // normalisation only by P's rounding (2^-9 bf16, 2^-4 e4m3).
+#pragma unroll
+        for (int k = 0; k < kTile; ++k) x[k] = exp2f(x[k] - m);
         float psum = 0.f;
+#pragma unroll
+        for (int k = 0; k < kTile; ++k) psum += x[k];
+        l += psum;
+        uint32_t pk[16];
         if (FP8) {
 #pragma unroll
           for (int k = 0; k < 16; ++k)
-            pk[k] = pack_e4m3x4(exp2f(x[4 * k] - m), exp2f(x[4 * k + 1] - m),
-                                exp2f(x[4 * k + 2] - m), exp2f(x[4 * k + 3] - m), psum);
+            pk[k] = pack_e4m3x4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
         } else {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            pk[k] = pack_bf16(exp2f(x[2 * k] - m), exp2f(x[2 * k + 1] - m));
-            psum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
-          }
+          for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
         }
-        l += psum;
         tmem_st_x16(lane_base + kColS + kTile * sb, pk);
         if (pos0 + kTile > len) {
           // Cache rows past seq_len may hold anything (even NaN bits): zero
@@ -675,6 +720,7 @@ __global__ void __launch_bounds__(256)
 decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
                     const float *__restrict__ ws_o,
                     const float *__restrict__ ws_lse, Tout *out, float *lse) {
+  sm100::grid_dep_wait();   // partials of the decode grid
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int j = row >> 7, r = row & 127;
   if (j >= J) return;
@@ -790,8 +836,10 @@ int launch_decode(const void *q, const void *kv_cache, int B, int q_len, int H,
   if (cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            smem) != cudaSuccess)
     return MLA_ERR_CUDA;
-  decode_kernel<FP8><<<2 * a.groups, kThreads, smem, stream>>>(tm_kv, tm_q, a);
-  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+  if (launch_pdl(decode_kernel<FP8>, dim3(2 * a.groups), dim3(kThreads), smem, stream,
+                 tm_kv, tm_q, a) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 }  // namespace
@@ -848,6 +896,7 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.q = static_cast<const uint8_t *>(q);
+  a.kv = static_cast<const uint8_t *>(kv_cache);
   a.q_len = q_len;
   a.H = H;
   a.HG = HG;
@@ -868,11 +917,14 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
 
   const int64_t rows = static_cast<int64_t>(J) * 128;
   const dim3 mgrid(static_cast<unsigned>((rows + 7) / 8));
+  const int32_t *cplan = plan;
+  const float *cws_o = ws_o, *cws_lse = ws_lse;
+  cudaError_t e;
   if (out_dtype == MLA_BF16)
-    decode_merge_kernel<__nv_bfloat16><<<mgrid, 256, 0, stream>>>(
-        plan, J, H, HG, ws_o, ws_lse, static_cast<__nv_bfloat16 *>(out), lse);
+    e = launch_pdl(decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(256), 0, stream, cplan,
+                   J, H, HG, cws_o, cws_lse, static_cast<__nv_bfloat16 *>(out), lse);
   else
-    decode_merge_kernel<float><<<mgrid, 256, 0, stream>>>(
-        plan, J, H, HG, ws_o, ws_lse, static_cast<float *>(out), lse);
-  return launch_status();
+    e = launch_pdl(decode_merge_kernel<float>, mgrid, dim3(256), 0, stream, cplan, J, H,
+                   HG, cws_o, cws_lse, static_cast<float *>(out), lse);
+  return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

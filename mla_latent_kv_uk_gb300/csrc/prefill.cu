@@ -225,14 +225,16 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         m = tmax;
       }
       const float ms = m == -INFINITY ? 0.f : m;
+      // row sum of the unrounded probabilities (see the decode kernel)
       float psum = 0.f;
 #pragma unroll
       for (int c = 0; c < kBN; c += 64) {
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          pk[k] = pack2(exp2f(x[c + 2 * k] - ms), exp2f(x[c + 2 * k + 1] - ms));
-          psum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+          const float p0 = exp2f(x[c + 2 * k] - ms), p1 = exp2f(x[c + 2 * k + 1] - ms);
+          psum += p0 + p1;
+          pk[k] = pack2(p0, p1);
         }
         tmem_st_x32(lane_base + kColS + 128 * sb + c / 2, pk);
       }

@@ -96,6 +96,14 @@ __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map,
       : "memory");
 }
 
+// Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
+__device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
+                   reinterpret_cast<uint64_t>(src)),
+               "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map))
                : "memory");
@@ -105,6 +113,17 @@ __device__ __forceinline__ void prefetch_tmap(const CUtensorMap *map) {
 // async-proxy (TMA / tcgen05.mma) reads of the same bytes.
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------- programmatic dependent launch
+// Blocks until the preceding grid in the stream has completed and its
+// memory is visible (no-op when the launch did not opt into PDL).
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+// Lets the next grid in the stream (launched with PDL) be scheduled now.
+__device__ __forceinline__ void grid_dep_launch() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
 // ----------------------------------------------------------------- tcgen05

@@ -257,7 +257,9 @@ def shard_cache_interleaved(g, cache: torch.Tensor, block_table, ctx_lens, W: in
             local_tokens.append(sel)
         lens = np.array([len(s) for s in local_tokens], dtype=np.int32)
         bt, nb = paged_layout(g, lens, spare_frac=spare_frac)
-        sc = torch.zeros((nb,) + tuple(cache.shape[1:]), dtype=cache.dtype)
+        # index through an integer view: torch cannot index float8 on the CPU
+        raw = cache.view(torch.uint8) if cache.element_size() == 1 else cache
+        sc = torch.zeros((nb,) + tuple(cache.shape[1:]), dtype=raw.dtype)
         for r in range(B):
             ts = local_tokens[r]
             if len(ts) == 0:
@@ -265,12 +267,12 @@ def shard_cache_interleaved(g, cache: torch.Tensor, block_table, ctx_lens, W: in
             j = (ts // (I * W)) * I + ts % I
             assert np.array_equal(j, np.arange(len(ts)))
             src_blk = block_table[r, ts // BLOCK]
-            src = cache[torch.from_numpy(src_blk.astype(np.int64)),
-                        torch.from_numpy((ts % BLOCK).astype(np.int64))]
+            src = raw[torch.from_numpy(src_blk.astype(np.int64)),
+                      torch.from_numpy((ts % BLOCK).astype(np.int64))]
             dst_blk = bt[r, j // BLOCK]
             sc[torch.from_numpy(dst_blk.astype(np.int64)),
                torch.from_numpy((j % BLOCK).astype(np.int64))] = src
-        out.append((sc, bt, lens))
+        out.append((sc.view(cache.dtype) if cache.element_size() == 1 else sc, bt, lens))
     return out
 
 

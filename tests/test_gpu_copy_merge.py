@@ -129,6 +129,8 @@ def test_merge_states(m, S, T, H, D, pdt, odt):
         po[:, 0, 1] = float("nan")              # whose parts hold NaN
     out, lse = m.mla_merge_states(po.cuda(), torch.from_numpy(pl).cuda(), out_dtype=odt)
     ro, rl = O.merge_states(f64(po), pl.astype(np.float64))
-    assert max_abs(f64(out), ro) <= 1e-2
+    # fp32 arithmetic error plus, for a bf16 output, half an ulp of the result
+    tol = 1e-4 + (2.0 ** -8 * np.abs(ro) if odt == torch.bfloat16 else 0.0)
+    assert np.all(np.abs(f64(out) - ro) <= tol)
     d, finite = lse_close(lse.cpu().numpy(), rl, 1e-3)
     assert finite and d <= 1e-3
