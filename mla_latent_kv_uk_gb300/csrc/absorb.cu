@@ -2,17 +2,20 @@
 // value up-projection: per-head GEMMs on the 5th-generation tensor cores.
 //
 // Both are small per-head contractions whose cost is reading the weights
-// (W_UK_T / W_UV: H x 128 x 512 bf16 = 16 MiB at H = 128).  Each CTA owns
-// one (head, 128-row M tile, token tile): TMA streams 64-wide K chunks of
-// the weight and the activations into 128B-swizzled shared memory, one
-// thread issues tcgen05.mma (M = 128, N = token tile, K = 16 per
-// instruction) into a TMEM accumulator, and four epilogue warps read the
-// accumulator with tcgen05.ld (lane = M row) and write the output rows.
+// (W_UK_T / W_UV: H x 128 x 512 bf16 = 16 MiB at H = 128), so the kernels
+// are built to keep a whole per-head weight slice in flight: TMA streams it
+// into 128B-swizzled shared memory, one thread issues tcgen05.mma (M = 128,
+// N = token tile, K = 16) into TMEM, and four epilogue warps move the
+// accumulator through a shared-memory staging tile so that every output
+// row leaves as coalesced 16-byte stores.
 //
 //   absorb: ql^T[l, t] = sum_p W_UK_T[h][p, l] * q_nope[t, h, p]
-//           A = W_UK_T[h] chunk, MN-major (l contiguous); B = q_nope, K-major
+//           one CTA per (head, 256-wide latent half, <=256-token tile):
+//           two M=128 accumulators, A = W_UK_T[h] (MN-major, l contiguous),
+//           B = q_nope (K-major); all 64 KB of weights requested up front.
 //   v_up:   out^T[v, t] = sum_l W_UV[h][v, l] * o_lat[t, h, l]
-//           A = W_UV[h], K-major; B = o_lat, K-major
+//           one CTA per (head, token tile): A = W_UV[h] (K-major), B = o_lat
+//           (K-major), K = 512 streamed through a ring up to 8 deep.
 //
 // Sources: prhub digest of vLLM PR 45964, §实现拆解 5 (the W_UK_T BMM of the
 // decode branch); "DeepSeek MLA 在 DCP 分布式环境中的 Prefill 阶段解析",
@@ -30,12 +33,9 @@ namespace {
 
 using namespace sm100;
 
-enum Op { kAbsorb = 0, kVup = 1 };
-
-constexpr int kStages = 4;
 constexpr int kThreads = 192;  // warp 0 TMA, warp 1 MMA, warps 2..5 epilogue
-constexpr int kChunkK = 64;    // K elements per pipeline stage
-constexpr int kABytes = 128 * kChunkK * 2;  // one 128 x 64 bf16 A chunk
+constexpr int kBoxBytes64 = 64 * 128;   // 64 rows x 64 bf16 (8 KB)
+constexpr int kStageTokens = 32;        // epilogue staging granularity
 
 struct GemmArgs {
   int T, H, NT;            // tokens, heads, token tile (multiple of 16)
@@ -46,60 +46,65 @@ struct GemmArgs {
   int *err;
 };
 
-__device__ __forceinline__ void store_q(void *out, int dtype, int64_t idx,
-                                        float v, float q_scale) {
+__device__ __forceinline__ int esize(int dtype) {
+  return dtype == MLA_F32 ? 4 : dtype == MLA_BF16 ? 2 : 1;
+}
+
+// Writes v (the fp32 value) in `dtype` at byte address p.
+__device__ __forceinline__ void put(uint8_t *p, int dtype, float v, float q_scale) {
   if (dtype == MLA_BF16) {
-    static_cast<__nv_bfloat16 *>(out)[idx] = __float2bfloat16_rn(v);
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(v);
   } else if (dtype == MLA_F32) {
-    static_cast<float *>(out)[idx] = v;
+    *reinterpret_cast<float *>(p) = v;
   } else {
     // e4m3 of the correctly rounded fp32 quotient: RNE, saturate to 448
-    static_cast<__nv_fp8_storage_t *>(out)[idx] =
+    *reinterpret_cast<__nv_fp8_storage_t *>(p) =
         __nv_cvt_float_to_fp8(__fdiv_rn(v, q_scale), __NV_SATFINITE, __NV_E4M3);
   }
 }
 
-template <int OP>
+__device__ __forceinline__ void epi_bar() {
+  asm volatile("bar.sync 1, 128;" ::: "memory");
+}
+
+__host__ __device__ inline uint32_t tmem_cols_for(int n) {
+  return n <= 32 ? 32 : n <= 64 ? 64 : n <= 128 ? 128 : 256;
+}
+
+// ------------------------------------------------------------------ absorb
+// smem: A [2 K-chunks][4 l-blocks] of {64 l x 64 p} boxes (64 KB),
+//       B [2 K-chunks] of {64 p x NT t} (NT * 128 B each), staging 32 KB.
 __global__ void __launch_bounds__(kThreads, 1)
-head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
-                 const __grid_constant__ CUtensorMap tm_b, GemmArgs args) {
-  constexpr int KC = OP == kAbsorb ? 128 / kChunkK : 512 / kChunkK;
+absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
+              const __grid_constant__ CUtensorMap tm_q, GemmArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NT = args.NT;
-  const int b_bytes = NT * kChunkK * 2;
-  const int stage_bytes = kABytes + b_bytes;  // multiple of 1024 (NT % 16 == 0 -> 2 KB)
-  uint8_t *stages = smem;
-  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * stage_bytes);
-  uint64_t *empty = full + kStages;
-  uint64_t *done = empty + kStages;
-  uint64_t *drain = done + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
+  uint8_t *sm_a = smem;                          // 64 KB
+  uint8_t *sm_b = smem + 8 * kBoxBytes64;        // 2 * NT * 128
+  uint8_t *sm_o = sm_b + 2 * NT * 128;           // 32 tokens x 256 x 4 B
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_o + kStageTokens * 256 * 4);
+  uint64_t *full = bars, *done = bars + 1, *drain = bars + 2;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
-  const int warp = warp_id();
-  const int lane = lane_id();
-  // grid: absorb (latent chunk, head, token tile); v_up (head, token tile)
-  const int mchunk = OP == kAbsorb ? blockIdx.x : 0;
-  const int h = OP == kAbsorb ? blockIdx.y : blockIdx.x;
-  const int ttile = OP == kAbsorb ? blockIdx.z : blockIdx.y;
-  const int t0 = ttile * NT;
+  const int warp = warp_id(), lane = lane_id();
+  const int mh = blockIdx.x;          // latent half: l in [256 mh, 256 mh + 256)
+  const int h = blockIdx.y;
+  const int t0 = blockIdx.z * NT;
   const int ntok = min(NT, args.T - t0);
-  const uint32_t tmem_cols = NT <= 32 ? 32 : NT <= 64 ? 64 : NT <= 128 ? 128 : 256;
+  const uint32_t cols = tmem_cols_for(NT);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
-    }
+    mbar_init(full, 1);
     mbar_init(done, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, tmem_cols);
+    tmem_alloc(tmem_slot, 2 * cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -108,62 +113,38 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
-    prefetch_tmap(&tm_a);
-    prefetch_tmap(&tm_b);
-    int armed_last = -1;
-    for (int kc = 0; kc < KC; ++kc) {
-      const int s = kc % kStages;
-      if (kc >= kStages && !mbar_wait(&empty[s], ((kc / kStages) - 1) & 1, abort_flag))
-        break;
-      uint8_t *a_dst = stages + s * stage_bytes;
-      uint8_t *b_dst = a_dst + kABytes;
-      mbar_arrive_expect_tx(&full[s], stage_bytes);
-      armed_last = kc;
-      if (OP == kAbsorb) {
-        // W_UK_T viewed as [H*128 rows (p), 512 cols (l)]; box 64 l x 64 p
-        const int row = h * 128 + kc * kChunkK;
-        tma_load_2d(a_dst, &tm_a, &full[s], mchunk * 128, row);
-        tma_load_2d(a_dst + kABytes / 2, &tm_a, &full[s], mchunk * 128 + 64, row);
-      } else {
-        // W_UV viewed as [H*128 rows (v), 512 cols (l)]; box 64 l x 128 v
-        tma_load_2d(a_dst, &tm_a, &full[s], kc * kChunkK, h * 128);
-      }
-      // activations [T, H, K]: box {64 (k), 1 (h), NT (t)}
-      tma_load_3d(b_dst, &tm_b, &full[s], kc * kChunkK, h, t0);
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_q);
+    mbar_arrive_expect_tx(full, 8 * kBoxBytes64 + 2 * NT * 128);
+    for (int kc = 0; kc < 2; ++kc) {
+      for (int lb = 0; lb < 4; ++lb)   // W_UK_T as [H*128 rows (p), 512 cols (l)]
+        tma_load_2d(sm_a + (kc * 4 + lb) * kBoxBytes64, &tm_w, full,
+                    256 * mh + 64 * lb, h * 128 + 64 * kc);
+      tma_load_3d(sm_b + kc * NT * 128, &tm_q, full, 64 * kc, h, t0);
     }
-    if (*abort_flag) {
-      // let the copies this thread started land before the CTA exits
-      for (int kc = max(0, armed_last - kStages + 1); kc <= armed_last; ++kc) {
-        volatile int no_abort = 0;
-        mbar_wait(&full[kc % kStages], (kc / kStages) & 1, &no_abort);
-      }
+    if (!mbar_wait(full, 0, abort_flag)) {
+      volatile int no_abort = 0;
+      mbar_wait(full, 0, &no_abort);
     }
   } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    const uint32_t idesc = idesc_bf16(128, NT, OP == kAbsorb, false);
-    bool ok = true;
-    for (int kc = 0; kc < KC && ok; ++kc) {
-      const int s = kc % kStages;
-      ok = mbar_wait(&full[s], (kc / kStages) & 1, abort_flag);
-      if (!ok) break;
+    const uint32_t idesc = idesc_bf16(128, NT, true, false);
+    const bool ok = mbar_wait(full, 0, abort_flag);
+    if (ok) {
       tc_fence_after();
-      const uint32_t a_base = smem_u32(stages + s * stage_bytes);
-      const uint32_t b_base = a_base + kABytes;
+      const uint32_t a = smem_u32(sm_a), b = smem_u32(sm_b);
 #pragma unroll
-      for (int kk = 0; kk < kChunkK / 16; ++kk) {
-        uint64_t adesc, bdesc;
-        if (OP == kAbsorb) {
-          // MN-major A: rows = K (p), 128 B = 64 l per row; 8-row groups
-          // 1024 B apart (SBO); the two 64-l halves 8 KB apart (LBO).
-          adesc = sdesc(a_base + kk * 2048, kABytes / 2, 1024, kSwizzle128B);
-        } else {
-          adesc = sdesc(a_base + kk * 32, 16, 1024, kSwizzle128B);
-        }
-        bdesc = sdesc(b_base + kk * 32, 16, 1024, kSwizzle128B);
-        mma_f16_ss(tmem, adesc, bdesc, idesc, (kc | kk) != 0);
-      }
-      mma_commit(&empty[s]);
+      for (int mc = 0; mc < 2; ++mc)
+#pragma unroll
+        for (int kc = 0; kc < 2; ++kc)
+#pragma unroll
+          for (int kk = 0; kk < 4; ++kk) {
+            // MN-major A: 128 B rows = 64 l of one p; 8-p groups 1024 B apart
+            // (SBO); the two 64-l blocks of this M chunk one box apart (LBO)
+            const uint64_t adesc = sdesc(a + (kc * 4 + 2 * mc) * kBoxBytes64 + kk * 2048,
+                                         kBoxBytes64, 1024, kSwizzle128B);
+            const uint64_t bdesc = sdesc(b + kc * NT * 128 + kk * 32, 16, 1024, kSwizzle128B);
+            mma_f16_ss(tmem + mc * cols, adesc, bdesc, idesc, (kc | kk) != 0);
+          }
     }
     mma_commit(ok ? done : drain);
     if (!ok) {
@@ -171,41 +152,49 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
       mbar_wait(drain, 0, &no_abort);
     }
   } else if (warp >= 2) {
-    // ---------------- epilogue: TMEM lane = M row, columns = tokens
+    const int tid = threadIdx.x - 64;
+    const int quarter = warp & 3;
+    const int lrow = quarter * 32 + lane;       // latent row within an M chunk
+    const int dt = args.out_dtype, es = esize(dt);
     const bool ok = mbar_wait(done, 0, abort_flag);
     tc_fence_after();
-    const int quarter = warp & 3;
-    const int m = quarter * 32 + lane;  // M row owned by this thread
     if (ok) {
-      for (int c0 = 0; c0 < NT; c0 += 32) {
-        uint32_t r[32];
-        tmem_ld_x32(tmem_addr(tmem, warp, c0), r);
-        const int nc = min(32, ntok - c0);
+      const int row_bytes = 256 * es;           // this CTA's half of a token row
+      for (int c0 = 0; c0 < ntok; c0 += kStageTokens) {
+        for (int mc = 0; mc < 2; ++mc) {
+          uint32_t r[32];
+          tmem_ld_x32(tmem_addr(tmem, warp, mc * cols + c0), r);
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          if (c >= nc) break;
-          const int t = t0 + c0 + c;
-          const float v = __uint_as_float(r[c]);
-          if (OP == kAbsorb) {
-            const int64_t idx = (static_cast<int64_t>(t) * args.H + h) * kDqk +
-                                mchunk * 128 + m;
-            store_q(args.out, args.out_dtype, idx, v, args.q_scale);
-          } else {
-            const int64_t idx = (static_cast<int64_t>(t) * args.H + h) * kVhead + m;
-            static_cast<__nv_bfloat16 *>(args.out)[idx] = __float2bfloat16_rn(v);
-          }
+          for (int c = 0; c < 32; ++c)
+            put(sm_o + c * row_bytes + (mc * 128 + lrow) * es, dt, __uint_as_float(r[c]),
+                args.q_scale);
         }
+        epi_bar();
+        const int nt = min(kStageTokens, ntok - c0);
+        const int chunks = row_bytes / 16;
+        uint8_t *out = static_cast<uint8_t *>(args.out);
+        for (int i = tid; i < nt * chunks; i += 128) {
+          const int t = t0 + c0 + i / chunks, c = i % chunks;
+          const int64_t base = ((static_cast<int64_t>(t) * args.H + h) * kDqk + 256 * mh) * es;
+          reinterpret_cast<uint4 *>(out + base)[c] =
+              reinterpret_cast<const uint4 *>(sm_o + (i / chunks) * row_bytes)[c];
+        }
+        epi_bar();
       }
-      if (OP == kAbsorb && mchunk == 0) {
-        // q_pe columns 512..575 of every token in the tile
-        const int tid = threadIdx.x - 64;
-        for (int idx = tid; idx < ntok * kRope; idx += 128) {
-          const int t = t0 + idx / kRope, r = idx % kRope;
-          const float v = __bfloat162float(
-              args.q_pe[(static_cast<int64_t>(t) * args.H + h) * kRope + r]);
-          store_q(args.out, args.out_dtype,
-                  (static_cast<int64_t>(t) * args.H + h) * kDqk + kLatent + r, v,
-                  args.q_scale);
+      if (mh == 1) {
+        // q_pe columns 512..575 of every token in the tile, 8 per thread
+        uint8_t *out = static_cast<uint8_t *>(args.out);
+        for (int i = tid; i < ntok * 8; i += 128) {
+          const int t = t0 + i / 8, c = (i % 8) * 8;
+          const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
+              args.q_pe + (static_cast<int64_t>(t) * args.H + h) * kRope + c));
+          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+          const int64_t base = ((static_cast<int64_t>(t) * args.H + h) * kDqk + kLatent + c) * es;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const float v = __uint_as_float((k & 1) ? (w[k >> 1] & 0xFFFF0000u) : (w[k >> 1] << 16));
+            put(out + base + k * es, dt, v, args.q_scale);
+          }
         }
       }
     }
@@ -215,17 +204,125 @@ head_gemm_kernel(const __grid_constant__ CUtensorMap tm_a,
   if (threadIdx.x == 0 && *abort_flag) raise_error(args.err, MLA_DEVERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, tmem_cols);
+    tmem_dealloc(tmem, 2 * cols);
+  }
+}
+
+// -------------------------------------------------------------------- v_up
+// smem: ring of stages {A: 64 l x 128 v (16 KB), B: 64 l x NT t}, staging.
+__global__ void __launch_bounds__(kThreads, 1)
+vup_kernel(const __grid_constant__ CUtensorMap tm_w,
+           const __grid_constant__ CUtensorMap tm_o, GemmArgs args, int stages) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int KC = 512 / 64;
+  const int NT = args.NT;
+  const int a_bytes = 128 * 128, stage_bytes = a_bytes + NT * 128;
+  uint8_t *sm_o = smem + stages * stage_bytes;          // 32 tokens x 256 B
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_o + kStageTokens * 256);
+  uint64_t *full = bars, *empty = bars + 8, *done = bars + 16, *drain = bars + 17;
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  const int warp = warp_id(), lane = lane_id();
+  const int h = blockIdx.x;
+  const int t0 = blockIdx.y * NT;
+  const int ntok = min(NT, args.T - t0);
+  const uint32_t cols = tmem_cols_for(NT);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(done, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, cols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_o);
+    int armed = -1;
+    for (int kc = 0; kc < KC; ++kc) {
+      const int s = kc % stages;
+      if (kc >= stages && !mbar_wait(&empty[s], ((kc / stages) - 1) & 1, abort_flag)) break;
+      uint8_t *dst = smem + s * stage_bytes;
+      mbar_arrive_expect_tx(&full[s], stage_bytes);
+      tma_load_2d(dst, &tm_w, &full[s], kc * 64, h * 128);  // W_UV [H*128 (v), 512 (l)]
+      tma_load_3d(dst + a_bytes, &tm_o, &full[s], kc * 64, h, t0);
+      armed = kc;
+    }
+    if (*abort_flag) {
+      volatile int no_abort = 0;
+      for (int kc = max(0, armed - stages + 1); kc <= armed; ++kc)
+        mbar_wait(&full[kc % stages], (kc / stages) & 1, &no_abort);
+    }
+  } else if (warp == 1 && lane == 0) {
+    const uint32_t idesc = idesc_bf16(128, NT, false, false);
+    bool ok = true;
+    for (int kc = 0; kc < KC; ++kc) {
+      const int s = kc % stages;
+      if (!(ok = mbar_wait(&full[s], (kc / stages) & 1, abort_flag))) break;
+      tc_fence_after();
+      const uint32_t a = smem_u32(smem + s * stage_bytes), b = a + a_bytes;
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk)
+        mma_f16_ss(tmem, sdesc(a + kk * 32, 16, 1024, kSwizzle128B),
+                   sdesc(b + kk * 32, 16, 1024, kSwizzle128B), idesc, (kc | kk) != 0);
+      mma_commit(&empty[s]);
+    }
+    mma_commit(ok ? done : drain);
+    if (!ok) {
+      volatile int no_abort = 0;
+      mbar_wait(drain, 0, &no_abort);
+    }
+  } else if (warp >= 2) {
+    const int tid = threadIdx.x - 64;
+    const int v = (warp & 3) * 32 + lane;
+    const bool ok = mbar_wait(done, 0, abort_flag);
+    tc_fence_after();
+    if (ok) {
+      for (int c0 = 0; c0 < ntok; c0 += kStageTokens) {
+        uint32_t r[32];
+        tmem_ld_x32(tmem_addr(tmem, warp, c0), r);
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+          reinterpret_cast<__nv_bfloat16 *>(sm_o + c * 256)[v] =
+              __float2bfloat16_rn(__uint_as_float(r[c]));
+        epi_bar();
+        const int nt = min(kStageTokens, ntok - c0);
+        for (int i = tid; i < nt * 16; i += 128) {
+          const int t = t0 + c0 + i / 16, c = i % 16;
+          reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.out) +
+                                    (static_cast<int64_t>(t) * args.H + h) * kVhead)[c] =
+              reinterpret_cast<const uint4 *>(sm_o + (i / 16) * 256)[c];
+        }
+        epi_bar();
+      }
+    }
+    tc_fence_before();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && *abort_flag) raise_error(args.err, MLA_DEVERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, cols);
   }
 }
 
 int token_tile(int T) {
   int nt = ((T + 15) / 16) * 16;
   return nt > 256 ? 256 : nt;
-}
-
-size_t smem_bytes(int NT) {
-  return 1024 + static_cast<size_t>(kStages) * (kABytes + NT * kChunkK * 2) + 256;
 }
 
 }  // namespace
@@ -243,7 +340,8 @@ extern "C" int mla_absorb_q(const void *q_nope, const void *q_pe,
     return MLA_ERR_INVALID_ARG;
   if (T == 0) return MLA_OK;
   if (!q_nope || !q_pe || !w_uk_t || !q_out) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(q_nope) || !aligned16(w_uk_t)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q_nope) || !aligned16(q_pe) || !aligned16(w_uk_t) || !aligned16(q_out))
+    return MLA_ERR_INVALID_ARG;
   int *err = device_error_word();
   if (!err) return MLA_ERR_CUDA;
   const int NT = token_tile(T);
@@ -268,13 +366,12 @@ extern "C" int mla_absorb_q(const void *q_nope, const void *q_pe,
   }
   GemmArgs a{T, H, NT, out_dtype, q_scale,
              static_cast<const __nv_bfloat16 *>(q_pe), q_out, err};
-  const size_t smem = smem_bytes(NT);
-  auto kern = head_gemm_kernel<kAbsorb>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const size_t smem = 1024 + 8 * kBoxBytes64 + 2 * NT * 128 + kStageTokens * 256 * 4 + 64;
+  if (cudaFuncSetAttribute(absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MLA_ERR_CUDA;
-  dim3 grid(kLatent / 128, H, (T + NT - 1) / NT);
-  kern<<<grid, kThreads, smem, stream>>>(ta, tb, a);
+  dim3 grid(2, H, (T + NT - 1) / NT);
+  absorb_kernel<<<grid, kThreads, smem, stream>>>(ta, tb, a);
   return launch_status();
 }
 
@@ -283,7 +380,7 @@ extern "C" int mla_v_up(const void *o_lat, const void *w_uv, int T, int H,
   if (T < 0 || H < 1 || H > 4096) return MLA_ERR_INVALID_ARG;
   if (T == 0) return MLA_OK;
   if (!o_lat || !w_uv || !out) return MLA_ERR_INVALID_ARG;
-  if (!aligned16(o_lat) || !aligned16(w_uv)) return MLA_ERR_INVALID_ARG;
+  if (!aligned16(o_lat) || !aligned16(w_uv) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
   int *err = device_error_word();
   if (!err) return MLA_ERR_CUDA;
   const int NT = token_tile(T);
@@ -308,12 +405,14 @@ extern "C" int mla_v_up(const void *o_lat, const void *w_uv, int T, int H,
       return MLA_ERR_CUDA;
   }
   GemmArgs a{T, H, NT, MLA_BF16, 1.f, nullptr, out, err};
-  const size_t smem = smem_bytes(NT);
-  auto kern = head_gemm_kernel<kVup>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  const int stage_bytes = 128 * 128 + NT * 128;
+  int stages = (200 * 1024) / stage_bytes;
+  stages = stages > 8 ? 8 : stages;
+  const size_t smem = 1024 + static_cast<size_t>(stages) * stage_bytes + kStageTokens * 256 + 256;
+  if (cudaFuncSetAttribute(vup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MLA_ERR_CUDA;
   dim3 grid(H, (T + NT - 1) / NT);
-  kern<<<grid, kThreads, smem, stream>>>(ta, tb, a);
+  vup_kernel<<<grid, kThreads, smem, stream>>>(ta, tb, a, stages);
   return launch_status();
 }

@@ -570,7 +570,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
     bool have = walk.next(sg);
     if (have) load_q_tmem(sg);
     while (ok && have) {
-      float m = -INFINITY, l = 0.f;
+      float m = -INFINITY, l = 0.f, lq = 0.f;
       const int len = __ldg(args.seq_lens + sg.b);
       for (int t = 0; t < sg.ntiles; ++t, ++uc) {
         const int sb = uc & 1;
@@ -611,29 +611,43 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
               tmem_st_x32(lane_base + kColO + c, o);
             }
             l *= alpha;
+            lq *= alpha;
             if (need) m = m_new;
           }
         } else {
           m = tmax;
         }
-        // The row sum uses the unrounded fp32 probabilities: the LSE then
-        // carries no rounding of P, and O / l differs from the exact
-        // normalisation only by P's rounding (2^-9 bf16, 2^-4 e4m3).
+        // Two row sums: `l` of the unrounded fp32 probabilities gives the
+        // LSE (no rounding of P in it); `lq` of the rounded values that the
+        // P.V MMA actually consumes normalises O, so O stays a convex
+        // combination of the value rows.
 #pragma unroll
         for (int k = 0; k < kTile; ++k) x[k] = exp2f(x[k] - m);
-        float psum = 0.f;
+        float psum = 0.f, qsum = 0.f;
 #pragma unroll
         for (int k = 0; k < kTile; ++k) psum += x[k];
         l += psum;
         uint32_t pk[16];
         if (FP8) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
+          for (int k = 0; k < 16; ++k) {
             pk[k] = pack_e4m3x4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+            __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>(pk[k] & 0xFFFFu), __NV_E4M3);
+            __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(
+                static_cast<__nv_fp8x2_storage_t>(pk[k] >> 16), __NV_E4M3);
+            const float2 f0 = __half22float2(*reinterpret_cast<__half2 *>(&h0));
+            const float2 f1 = __half22float2(*reinterpret_cast<__half2 *>(&h1));
+            qsum += (f0.x + f0.y) + (f1.x + f1.y);
+          }
         } else {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
+          for (int k = 0; k < 16; ++k) {
+            pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
+            qsum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+          }
         }
+        lq += qsum;
         tmem_st_x16(lane_base + kColS + kTile * sb, pk);
         if (pos0 + kTile > len) {
           // Cache rows past seq_len may hold anything (even NaN bits): zero
@@ -666,7 +680,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
       have = walk.next(sg);
       if (have) load_q_tmem(sg);
       // ---- epilogue: O / l for this CTA's 256 latent columns
-      const float inv = args.out_scale / l;
+      const float inv = args.out_scale / lq;
       const bool row_ok = r < cur.hrows;
       const int64_t orow = static_cast<int64_t>(cur.out_row0 + r);
 #pragma unroll 1

@@ -162,7 +162,8 @@ def test_decode_fp32_out_and_head_groups(m):
     case = synth.decode_case("hg", 441, B=2, H=200, seq_lens=[77, 300], poison=True)
     out, lse = _run_decode(m, case, out_dtype=torch.float32, split_tiles=2)
     ro, rl = _oracle_decode(case)
-    _check(out, lse, ro, rl, out_tol=1e-3)
+    # an fp32 output drops only the final bf16 rounding; P is still bf16
+    _check(out, lse, ro, rl)
 
 
 def test_decode_causal_pair(m):
