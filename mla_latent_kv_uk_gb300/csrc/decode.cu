@@ -331,8 +331,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
   uint64_t *kv_empty = bars + kStages;      // [kStages]
   uint64_t *s_full = bars + 2 * kStages;    // [2]
   uint64_t *p_full = s_full + 2;            // [2]
-  uint64_t *pv_done = p_full + 2;
-  uint64_t *q_full = pv_done + 1;
+  uint64_t *pv_done = p_full + 2;           // [2], one per S/P buffer
+  uint64_t *q_full = pv_done + 2;
   uint64_t *q_tmem = q_full + 1;
   uint64_t *q_free = q_tmem + 1;
   uint64_t *drain = q_free + 1;
@@ -352,7 +352,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 128);
     }
-    mbar_init(pv_done, 1);
+    mbar_init(&pv_done[0], 1);
+    mbar_init(&pv_done[1], 1);
     mbar_init(q_full, 1);
     mbar_init(q_tmem, 128);
     mbar_init(q_free, 1);
@@ -525,7 +526,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
             else mma_f16_ts(tmem + kColO, a, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&kv_empty[kc % kStages]);
-          mma_commit(pv_done);
+          mma_commit(&pv_done[uc & 1]);
           if (t + 1 == sg.ntiles) mma_commit(q_free);
         }
       }
@@ -541,7 +542,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
     const int r = quarter * 32 + lane;  // head row within the group
     const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
     const int tid = threadIdx.x - 64;   // 0..127
-    int uc = 0, npv = 0;
+    int uc = 0;
     bool ok = true;
     // Query dims 0..383 of row r of segment `seg` -> TMEM [kColQ, kColQ+192).
     // Done for the next segment as soon as the previous one's MMAs are over
@@ -593,13 +594,17 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
           }
         }
         if (t > 0) {
-          ok = mbar_wait(pv_done, npv & 1, abort_flag);
-          ++npv;
-          if (!ok) break;
-          tc_fence_after();
           const float m_new = fmaxf(m, tmax);
           const bool need = m_new > m + kRescaleLog2;
           if (__any_sync(0xffffffffu, need)) {
+            // O may only be rescaled once PV(t-1) has landed.  PV completions
+            // are committed to the barrier of their S/P buffer, so the
+            // barrier of tile t-1 is at most one phase ahead of this wait
+            // and skipped waits on tiles without a rescale are harmless.
+            const int up = uc - 1;
+            ok = mbar_wait(&pv_done[up & 1], (up >> 1) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
             const float alpha = need ? exp2f(m - m_new) : 1.f;
 #pragma unroll 1
             for (int c = 0; c < 256; c += 32) {
@@ -671,8 +676,10 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         mbar_arrive(&p_full[sb]);
       }
       if (!ok) break;
-      ok = mbar_wait(pv_done, npv & 1, abort_flag);
-      ++npv;
+      {
+        const int up = uc - 1;  // the last PV of this segment (all earlier ones are done too)
+        ok = mbar_wait(&pv_done[up & 1], (up >> 1) & 1, abort_flag);
+      }
       if (!ok) break;
       tc_fence_after();
       // every MMA of this segment is done: stage the next segment's query

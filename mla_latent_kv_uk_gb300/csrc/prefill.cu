@@ -75,7 +75,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm_kv + kStages * kStageBytes);
   uint64_t *kv_full = bars, *kv_empty = bars + kStages;
   uint64_t *s_full = bars + 2 * kStages, *p_full = s_full + 2;
-  uint64_t *pv_done = p_full + 2, *q_full = pv_done + 1, *drain = q_full + 1;
+  uint64_t *pv_done = p_full + 2;             // [2], one per S/P buffer
+  uint64_t *q_full = pv_done + 2, *drain = q_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   const int warp = warp_id(), lane = lane_id();
@@ -89,7 +90,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 128);
     }
-    mbar_init(pv_done, 1);
+    mbar_init(&pv_done[0], 1);
+    mbar_init(&pv_done[1], 1);
     mbar_init(q_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -170,7 +172,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    sdesc(vb + kk * 2048, kBox, 1024, kSwizzle128B), idesc_pv,
                    (t > 0 || kk > 0) ? 1u : 0u);
       mma_commit(&kv_empty[t % kStages]);
-      mma_commit(pv_done);
+      mma_commit(&pv_done[t & 1]);
     }
     if (!ok) {
       mma_commit(drain);
@@ -203,11 +205,13 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         }
       }
       if (t > 0) {
-        if (!(ok = mbar_wait(pv_done, (t - 1) & 1, abort_flag))) break;
-        tc_fence_after();
         const float m_new = fmaxf(m, tmax);
         const bool need = m_new > m + kRescaleLog2 || (m == -INFINITY && m_new > -INFINITY);
         if (__any_sync(0xffffffffu, need)) {
+          // rescale only after PV(t-1) landed; per-buffer barriers are never
+          // more than one phase ahead of this wait (see the decode kernel)
+          if (!(ok = mbar_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag))) break;
+          tc_fence_after();
           const float alpha = need ? (m == -INFINITY ? 0.f : exp2f(m - m_new)) : 1.f;
 #pragma unroll 1
           for (int c = 0; c < kDv; c += 32) {
@@ -242,7 +246,8 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       tc_fence_before();
       mbar_arrive(&p_full[sb]);
     }
-    if (ok && ntiles > 0) ok = mbar_wait(pv_done, (ntiles - 1) & 1, abort_flag);
+    if (ok && ntiles > 0)
+      ok = mbar_wait(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag);
     tc_fence_after();
     if (ok) {
       const bool row_ok = r < rows;
