@@ -137,6 +137,38 @@ int mla_decode_paged(const void *q, int q_dtype, float q_scale,
                      int out_dtype, float *lse, void *workspace,
                      size_t ws_bytes, mla_stream_t stream);
 
+/* mla_decode_paged without a caller workspace, for callers that cannot
+ * allocate device memory at call time: serving runtimes whose device
+ * memory is carved up once before traffic starts, plug-in hosts that forbid
+ * allocation on the call path, and C callers with no allocator of their
+ * own.  No counterpart on the source pages: it is a packaging
+ * variant of A3/A4/A5.
+ *
+ * The plan and the split partials live in one static device array of
+ * MLA_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library; every GPU that
+ * loads the library holds it until the process exits.  Requests whose
+ * workspace (mla_decode_workspace_size with max_seq_len = max_blocks*64)
+ * exceeds that size are rejected with MLA_ERR_WORKSPACE.  The library never
+ * allocates here: no cudaMalloc, cudaFree or allocating library routine.
+ * The first call on a device looks the array's device address up once
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that
+ * first call before any stream capture.  Every call shares the one array,
+ * so calls that overlap on the GPU (different streams, or devices sharing a
+ * context) race and must be serialised by the caller.  Nothing in the array
+ * needs to start at zero: the plan is rewritten and every partial is
+ * written before it is read on each call.  Arguments and results are those
+ * of mla_decode_paged. */
+#define MLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+int mla_decode_paged_noalloc(const void *q, int q_dtype, float q_scale,
+                             const void *kv_cache, int kv_dtype, float k_scale,
+                             const int32_t *block_table,
+                             const int32_t *seq_lens, const int32_t *kv_starts,
+                             const int32_t *kv_ends, int B, int q_len, int H,
+                             int max_blocks, int num_blocks, float sm_scale,
+                             int causal, int split_tiles, void *out,
+                             int out_dtype, float *lse, mla_stream_t stream);
+
 /* A3 on its own: writes the split plan that mla_decode_paged computes.
  * Jobs are (b, i, head group of 128) in that nesting order; with the tile
  * size tk = 32 tokens (kv_dtype MLA_BF16) or 64 tokens (MLA_E4M3), job j

@@ -39,6 +39,8 @@ _SIGNATURES = {
     "mla_decode_workspace_size": ([_i, _i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
     "mla_decode_paged": ([_p, _i, _f, _p, _i, _f, _p, _p, _p, _p, _i, _i, _i, _i,
                           _i, _f, _i, _i, _p, _i, _p, _p, _sz, _p], _i),
+    "mla_decode_paged_noalloc": ([_p, _i, _f, _p, _i, _f, _p, _p, _p, _p, _i, _i, _i, _i,
+                                  _i, _f, _i, _i, _p, _i, _p, _p], _i),
     "mla_decode_plan": ([_p, _p, _p, _i, _i, _i, _i, _i, _i, _i, _i, _p, _sz, _p], _i),
     "mla_merge_states": ([_p, _i, _p, _i, _i, _i, _i, _p, _i, _p, _p], _i),
     "mla_v_up": ([_p, _p, _i, _i, _p, _p], _i),

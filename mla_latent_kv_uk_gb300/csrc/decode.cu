@@ -32,6 +32,8 @@
 #include <cuda_fp8.h>
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "merge_row.cuh"
 #include "sm100.cuh"
@@ -948,4 +950,49 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
     e = launch_pdl(decode_merge_kernel<float>, mgrid, dim3(256), 0, stream, cplan, J, H,
                    HG, cws_o, cws_lse, static_cast<float *>(out), lse);
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
+
+// ------------------------------------------------- no-allocation variant
+namespace {
+
+// Scratch of mla_decode_paged_noalloc: the plan and the split partials.
+static __device__ __align__(256) uint8_t g_noalloc_scratch[MLA_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (in host code the symbol is only a stand-in, not an address).
+void *noalloc_scratch() {
+  constexpr int kMaxDev = 64;
+  static std::mutex mu;
+  static void *addr[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!addr[dev]) {
+    void *p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" int mla_decode_paged_noalloc(
+    const void *q, int q_dtype, float q_scale, const void *kv_cache, int kv_dtype,
+    float k_scale, const int32_t *block_table, const int32_t *seq_lens,
+    const int32_t *kv_starts, const int32_t *kv_ends, int B, int q_len, int H,
+    int max_blocks, int num_blocks, float sm_scale, int causal, int split_tiles,
+    void *out, int out_dtype, float *lse, mla_stream_t stream) {
+  if (!decode_shape_ok(B, q_len, H) || max_blocks < 1 || split_tiles < 0 ||
+      static_cast<int64_t>(max_blocks) * kPage > (1ll << 30))
+    return MLA_ERR_INVALID_ARG;
+  const WsLayout w = ws_layout(B, q_len, H, max_blocks * kPage, split_tiles,
+                               groups_for_device());
+  if (w.total > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;
+  void *ws = noalloc_scratch();
+  if (!ws) return MLA_ERR_CUDA;
+  return mla_decode_paged(q, q_dtype, q_scale, kv_cache, kv_dtype, k_scale,
+                          block_table, seq_lens, kv_starts, kv_ends, B, q_len, H,
+                          max_blocks, num_blocks, sm_scale, causal, split_tiles, out,
+                          out_dtype, lse, ws, MLA_NOALLOC_SCRATCH_BYTES, stream);
 }
