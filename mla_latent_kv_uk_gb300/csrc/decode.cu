@@ -277,7 +277,6 @@ struct DecodeArgs {
   const int32_t *block_table;
   const int32_t *seq_lens;
   const uint8_t *q;           // [B, q_len, H, 576] bf16 or e4m3
-  const uint8_t *kv;          // [num_blocks, 64, 576] (L2 prefetch source)
   int q_len, H, HG, max_blocks, num_blocks, groups;
   float scale_log2;           // sm_scale * log2(e) (* q_scale * k_scale)
   float out_scale;            // 1 (bf16) or k_scale (e4m3 values)
@@ -384,14 +383,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
     // The whole warp walks the work; lane 0 issues barrier and TMA
     // operations.  Block-table entries are fetched 32 pages at a time (one
     // per lane) and broadcast with shuffles, so no tile waits on a global
-    // load; CTA half 0 also prefetches tiles kPrefetch ahead into L2, where
-    // the TMA loads of both CTAs of the pair find them.
+    // load.
     if (lane == 0) {
       prefetch_tmap(&tm_kv);
       prefetch_tmap(&tm_q);
     }
-    constexpr int kPrefetch = 16;
-    constexpr int kRowBytes = FP8 ? kDqk : kDqk * 2;
     int kc = 0, nseg = 0;
     bool ok = true;
     while (ok && walk.next(sg)) {
@@ -407,18 +403,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
       };
       auto row_of = [&](int tile, int blk) -> int {
         return blk * kPage + (tile * kTile) % kPage;
-      };
-      int pf = 0;  // tiles of this segment prefetched so far
-      auto prefetch_upto = [&](int t_end) {
-        t_end = min(t_end, sg.ntiles);
-        while (pf < t_end) {
-          const int tile = sg.tile0 + pf;
-          const int blk = blk_of(tile);
-          if (half == 0 && lane == 0 && blk >= 0 && blk < args.num_blocks)
-            prefetch_l2(args.kv + static_cast<int64_t>(row_of(tile, blk)) * kRowBytes,
-                        kStageBytes);
-          ++pf;
-        }
       };
       // Loads KV tile `tile` into ring slot kc % kStages.
       auto load_tile = [&](int tile) -> bool {
@@ -442,7 +426,6 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         ++kc;
         return true;
       };
-      prefetch_upto(kPrefetch);
       // The first ring-full of this segment's tiles only needs free ring
       // slots; the query slot frees when the previous segment's MMAs end.
       const int pre = min(sg.ntiles, kStages);
@@ -455,10 +438,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
           tma_load_2d(sm_q + k * kQBox, &tm_q, q_full, kQsFirstCol + 64 * k, sg.row0);
       }
       ++nseg;
-      for (int t = pre; ok && t < sg.ntiles; ++t) {
-        prefetch_upto(t + kPrefetch);
-        ok = load_tile(sg.tile0 + t);
-      }
+      for (int t = pre; ok && t < sg.ntiles; ++t) ok = load_tile(sg.tile0 + t);
     }
     if (*abort_flag && lane == 0) {
       volatile int no_abort = 0;
@@ -507,14 +487,27 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         tc_fence_after();
         issue_qk(kc, uc);
         for (int t = 0; t < sg.ntiles; ++t, ++kc, ++uc) {
-          if (t + 1 < sg.ntiles) {
-            ok = mbar_wait(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            issue_qk(kc + 1, uc + 1);
+          // QK(t+1) and PV(t) are independent (different TMEM columns and
+          // inputs): issue each as soon as its input is there, so a late
+          // KV tile never holds back PV(t) and the release of ring slot t.
+          bool qk_next = t + 1 >= sg.ntiles;   // nothing to issue
+          bool pv_now = false;
+          long long t_spin = 0;
+          while (!pv_now) {
+            if (!qk_next && mbar_try_wait(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1)) {
+              tc_fence_after();
+              issue_qk(kc + 1, uc + 1);
+              qk_next = true;
+            }
+            if (mbar_try_wait(&p_full[uc & 1], (uc >> 1) & 1)) {
+              pv_now = true;
+              break;
+            }
+            if (*abort_flag) break;
+            if (t_spin == 0) t_spin = clock64();
+            else if (clock64() - t_spin > kWaitLimitCycles) { *abort_flag = 1; break; }
           }
-          ok = mbar_wait(&p_full[uc & 1], (uc >> 1) & 1, abort_flag);
-          if (!ok) break;
+          if (!pv_now) { ok = false; break; }
           tc_fence_after();
           const uint32_t stage = smem_u32(sm_kv + (kc % kStages) * kStageBytes);
 #pragma unroll
@@ -530,6 +523,12 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
           mma_commit(&kv_empty[kc % kStages]);
           mma_commit(&pv_done[uc & 1]);
           if (t + 1 == sg.ntiles) mma_commit(q_free);
+          if (!qk_next) {
+            ok = mbar_wait(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1, abort_flag);
+            if (!ok) break;
+            tc_fence_after();
+            issue_qk(kc + 1, uc + 1);
+          }
         }
       }
       if (!ok) {
@@ -919,7 +918,6 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   a.block_table = block_table;
   a.seq_lens = seq_lens;
   a.q = static_cast<const uint8_t *>(q);
-  a.kv = static_cast<const uint8_t *>(kv_cache);
   a.q_len = q_len;
   a.H = H;
   a.HG = HG;
