@@ -494,12 +494,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
           bool pv_now = false;
           long long t_spin = 0;
           while (!pv_now) {
-            if (!qk_next && mbar_try_wait(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1)) {
+            // test_wait never suspends: a missing KV tile must not delay
+            // noticing P(t) (try_wait may sleep until its barrier flips)
+            if (!qk_next && mbar_test(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1)) {
               tc_fence_after();
               issue_qk(kc + 1, uc + 1);
               qk_next = true;
             }
-            if (mbar_try_wait(&p_full[uc & 1], (uc >> 1) & 1)) {
+            if (mbar_test(&p_full[uc & 1], (uc >> 1) & 1)) {
               pv_now = true;
               break;
             }
