@@ -180,6 +180,29 @@ def run_ours(args, rank, world, device):
         e2.record(stream)
         m.mla_v_up(o_lat.view(T, H, 512), d["w_uv"], out=y)
 
+    def breakdown(k):
+        """Per-call device times (ms) of the three entry points, each after an
+        L2 flush (so each starts cold, as inside a real step)."""
+        names = ("absorb", "decode", "v_up")
+        calls = (
+            lambda: m.mla_absorb_q(d["q_nope"], d["q_pe"], d["w_uk_t"], out=q),
+            lambda: m.mla_decode_paged(q.view(B, 1, H, 576), d["cache"], d["bt"], d["sl"],
+                                       sm_scale=case.sm_scale, out=o_lat, lse=lse, workspace=ws),
+            lambda: m.mla_v_up(o_lat.view(T, H, 512), d["w_uv"], out=y))
+        res = {}
+        for nm, fn in zip(names, calls):
+            ts = []
+            for _ in range(k):
+                flush.zero_()
+                a0, a1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a0.record(stream)
+                fn()
+                a1.record(stream)
+                torch.cuda.synchronize()
+                ts.append(a0.elapsed_time(a1))
+            res[nm] = statistics.median(ts)
+        return res
+
     # host-buffer (end-to-end) variant: inputs copied from pinned host memory
     # and the result read back every step, all inside the timed region
     h_qn = d["q_nope"].cpu().pin_memory()
@@ -216,6 +239,7 @@ def run_ours(args, rank, world, device):
     if world > 1:
         torch.distributed.barrier()
     e2e_tot, _ = timed(e2e_step, args.steps, has_dec=False)
+    parts = breakdown(max(3, min(args.steps, 10)))
     err = m.mla_get_device_error()
 
     ms, ms_e2e, ms_dec = max_over_ranks(
@@ -240,6 +264,7 @@ def run_ours(args, rank, world, device):
                      "kernel_ms": ms_dec, "peak_source": src,
                      "tensor_tflops": flops / (ms_dec * 1e-3) / 1e12,
                      "tensor_frac_of_bf16_peak": flops / (ms_dec * 1e-3) / 1e12 / bf16},
+        "step_breakdown_ms": parts,
         "gpu_launches": 5 * args.steps,
         "clocks": clk.summary(),
         "device_error": err,
