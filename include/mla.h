@@ -119,8 +119,7 @@ int mla_absorb_q(const void *q_nope, const void *q_pe, const void *w_uk_t,
  * The split of the key ranges over CTAs is planned on the device
  * (mla_decode_plan) and partial results are merged on the device; no host
  * synchronisation.  split_tiles = 0 lets the planner choose; > 0 forces
- * spans of that many key tiles (32 tokens for bf16, 64 for e4m3; testing /
- * tuning).  workspace must
+ * spans of that many 64-token key tiles (testing / tuning).  workspace must
  * hold mla_decode_workspace_size(B, q_len, H, max_blocks*64, split_tiles)
  * bytes (16-byte aligned).
  * Limits: 1 <= B, 1 <= q_len <= 64, 1 <= H <= 4096, 1 <= max_blocks,
@@ -171,8 +170,9 @@ int mla_decode_paged_noalloc(const void *q, int q_dtype, float q_scale,
 
 /* A3 on its own: writes the split plan that mla_decode_paged computes.
  * Jobs are (b, i, head group of 128) in that nesting order; with the tile
- * size tk = 32 tokens (kv_dtype MLA_BF16) or 64 tokens (MLA_E4M3), job j
- * covers key tiles [lo/tk, ceil(hi/tk)); tiles of all jobs are
+ * size tk = 64 tokens (both kv dtypes; kv_dtype is kept so the tile may
+ * differ by format), job j covers key tiles [lo/tk, ceil(hi/tk)); tiles of
+ * all jobs are
  * concatenated into one flat space of `total` tiles, and CTA group p owns
  * flat tiles [p*C, (p+1)*C) with C = split_tiles if > 0, else
  * max(4, ceil(total / n_groups)).

@@ -10,22 +10,26 @@
 // §Chunked Prefill 与 LSE Merge (LSE-rescaling merge of partial states).
 //
 // Design (GB300, sm_103a):
-//  * All 128 heads of a query token share one latent KV row, so per 32-token
-//    tile S = Q K^T is a dense [128 x 32 x 576] contraction and O += P V a
-//    [128 x 256 x 32] one: both run on tcgen05 with fp32 TMEM accumulators.
+//  * All 128 heads of a query token share one latent KV row, so per 64-token
+//    tile S = Q K^T is a dense [128 x 64 x 576] contraction and O += P V a
+//    [128 x 256 x 64] one: both run on tcgen05 with fp32 TMEM accumulators.
+//    A tcgen05.mma with M = 128, K = 16 costs about the same to issue for
+//    any N up to 128 (measured), so the tile is as wide in tokens as shared
+//    memory allows.
 //  * The fp32 output of 128 heads x 512 latent columns is exactly one SM's
 //    TMEM, so each work span is processed by a PAIR of CTAs: CTA c owns
 //    latent columns [256c, 256c + 256) of O and recomputes S itself (the
 //    two CTAs read the same KV tiles; the second read is an L2 hit).
-//  * TMEM (512 columns): O half [0,256), S/P double buffer [256,320),
-//    query dims 0..383 as the MMA A operand [320,512).  Query dims
-//    384..575 stay in shared memory; the KV ring holds 4 tiles of 36 KB.
+//  * TMEM (512 columns), bf16: O half [0,256), S/P double buffer [256,384),
+//    query dims 0..255 as the QK A operand [384,512); query dims 256..575
+//    stay in shared memory next to a 2-deep ring of 72 KB KV tiles.  e4m3:
+//    the whole query in shared memory, a 4-deep ring of 36 KB tiles.
 //  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer (+ TMEM owner),
 //    warps 2..5 online softmax (one head row per thread), correction and
 //    epilogue.  Lazy rescaling: O is rescaled only when a row max grows by
 //    more than 2^8.
 //  * Work split (A3): every job (request, query token, 128-head group)
-//    contributes the 32-token tiles its key range touches; jobs are laid
+//    contributes the 64-token tiles its key range touches; jobs are laid
 //    end to end and CTA pair p takes flat tiles [p*C, (p+1)*C).  A job cut
 //    into several spans writes fp32 partials that a merge kernel combines.
 #include <cuda_bf16.h>
@@ -55,15 +59,15 @@ struct Geo;
 
 template <>
 struct Geo<false> {                          // bf16 cache and query
-  static constexpr int kTile = 32;           // tokens per KV tile
-  static constexpr int kStages = 4;
+  static constexpr int kTile = 64;           // tokens per KV tile (= MMA N)
+  static constexpr int kStages = 2;
   static constexpr int kRowBytes = 128;      // 64 bf16 per box row
-  static constexpr int kBox = kTile * kRowBytes;          // 4 KB
-  static constexpr int kStageBytes = 9 * kBox;            // 36 KB
+  static constexpr int kBox = kTile * kRowBytes;          // 8 KB
+  static constexpr int kStageBytes = 9 * kBox;            // 72 KB
   static constexpr int kQBox = 128 * kRowBytes;           // 16 KB
-  static constexpr int kQsBoxes = 3;         // query dims 384..575 in smem
-  static constexpr int kQtCols = 192;        // query dims 0..383 in TMEM
-  static constexpr uint32_t kColQ = 320;
+  static constexpr int kQsBoxes = 5;         // query dims 256..575 in smem
+  static constexpr int kQtCols = 128;        // query dims 0..255 in TMEM
+  static constexpr uint32_t kColQ = 384;
   static constexpr int kKStep = 16;          // K per MMA instruction
   static constexpr uint32_t kSwizzle = sm100::kSwizzle128B;
   static constexpr uint32_t kSBO = 1024;     // 8 rows x 128 B
@@ -547,7 +551,8 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
     const int tid = threadIdx.x - 64;   // 0..127
     int uc = 0;
     bool ok = true;
-    // Query dims 0..383 of row r of segment `seg` -> TMEM [kColQ, kColQ+192).
+    // Query dims [0, 2*kQtCols) of row r of segment `seg` -> TMEM columns
+    // [kColQ, kColQ + kQtCols) (two bf16 per 32-bit column).
     // Done for the next segment as soon as the previous one's MMAs are over
     // (before its epilogue), so the next QK MMAs overlap that epilogue.
     auto load_q_tmem = [&](const Seg &seg) {
@@ -555,7 +560,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         const uint4 *src = reinterpret_cast<const uint4 *>(
             args.q + static_cast<int64_t>(seg.row0 + r) * kDqk * 2);
         const bool valid = r < seg.hrows;
-        // 3 batches of 16 independent 16-byte loads (two TMEM stores each)
+        // batches of 16 independent 16-byte loads (two TMEM stores each)
 #pragma unroll 1
         for (int c = 0; c < G::kQtCols / 64; ++c) {
           uint32_t w[64];
@@ -635,10 +640,11 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
 #pragma unroll
         for (int k = 0; k < kTile; ++k) psum += x[k];
         l += psum;
-        uint32_t pk[16];
+        constexpr int kPCols = FP8 ? kTile / 4 : kTile / 2;   // 32-bit TMEM columns of P
+        uint32_t pk[kPCols];
         if (FP8) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
+          for (int k = 0; k < kPCols; ++k) {
             pk[k] = pack_e4m3x4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
             __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
                 static_cast<__nv_fp8x2_storage_t>(pk[k] & 0xFFFFu), __NV_E4M3);
@@ -650,13 +656,14 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
           }
         } else {
 #pragma unroll
-          for (int k = 0; k < 16; ++k) {
+          for (int k = 0; k < kPCols; ++k) {
             pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
             qsum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
           }
         }
         lq += qsum;
-        tmem_st_x16(lane_base + kColS + kTile * sb, pk);
+        if (kPCols == 32) tmem_st_x32(lane_base + kColS + kTile * sb, pk);
+        else tmem_st_x16(lane_base + kColS + kTile * sb, pk);
         if (pos0 + kTile > len) {
           // Cache rows past seq_len may hold anything (even NaN bits): zero
           // this CTA's value columns of those rows so that P = 0 really

@@ -102,7 +102,7 @@ def test_plan_matches_oracle(m, split_tiles, n_groups, fp8):
                 a, z = O.decode_range(int(seq[b]), q_len, i, True, starts[b], ends[b])
                 lo.append(a)
                 hi.append(z)
-    ref = O.decode_plan(lo, hi, n_groups, tile=64 if fp8 else 32, min_tiles=4,
+    ref = O.decode_plan(lo, hi, n_groups, tile=64, min_tiles=4,
                         forced_chunk=split_tiles)
     J = len(lo)
     assert plan[2] == J
