@@ -37,6 +37,7 @@
 #include <math.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "merge_row.cuh"
@@ -460,11 +461,21 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
       const uint32_t q_base = smem_u32(sm_q);
       int kc = 0, uc = 0, nseg = 0;
       bool ok = true;
-      auto issue_qk = [&](int kcx, int ucx) {
+      // QK of one tile is issued in kQkChunks pieces so the MMA thread can
+      // slip PV(t) in between as soon as P(t) is ready (a single thread
+      // needs ~60 cycles per tcgen05.mma, ~2,300 for a whole bf16 QK).
+      constexpr int kQkChunks = 4;
+      constexpr int kChunkSteps = (kQkSteps + kQkChunks - 1) / kQkChunks;
+      // `chunk_c` is a std::integral_constant so every descriptor offset
+      // below is a compile-time constant.
+      auto issue_qk_chunk_c = [&](int kcx, int ucx, auto chunk_c) {
+        constexpr int chunk = decltype(chunk_c)::value;
         const uint32_t stage = smem_u32(sm_kv + (kcx % kStages) * kStageBytes);
         const uint32_t d = tmem + kColS + kTile * (ucx & 1);
 #pragma unroll
-        for (int k = 0; k < kQkSteps; ++k) {
+        for (int j = 0; j < kChunkSteps; ++j) {
+          const int k = chunk * kChunkSteps + j;
+          if (k >= kQkSteps) break;
           const uint32_t off = (k / kStepsPerBox) * kBox + (k % kStepsPerBox) * 32;
           const uint64_t bdesc = sdesc(stage + off, 16, G::kSBO, G::kSwizzle);
           if (k < kTmemQSteps) {
@@ -478,7 +489,22 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
             else mma_f16_ss(d, adesc, bdesc, idesc_qk, k > 0);
           }
         }
-        mma_commit(&s_full[ucx & 1]);
+        if (chunk == kQkChunks - 1) mma_commit(&s_full[ucx & 1]);
+      };
+      auto issue_qk_chunk = [&](int kcx, int ucx, int chunk) {
+        static_assert(kQkChunks == 4, "dispatch below covers four chunks");
+        switch (chunk) {
+          case 0: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 0>{}); break;
+          case 1: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 1>{}); break;
+          case 2: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 2>{}); break;
+          default: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 3>{}); break;
+        }
+      };
+      auto issue_qk = [&](int kcx, int ucx) {
+        issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 0>{});
+        issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 1>{});
+        issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 2>{});
+        issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 3>{});
       };
       while (ok && walk.next(sg)) {
         // the query of this segment: smem part by TMA, TMEM part by softmax warps
@@ -492,49 +518,47 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         issue_qk(kc, uc);
         for (int t = 0; t < sg.ntiles; ++t, ++kc, ++uc) {
           // QK(t+1) and PV(t) are independent (different TMEM columns and
-          // inputs): issue each as soon as its input is there, so a late
-          // KV tile never holds back PV(t) and the release of ring slot t.
-          bool qk_next = t + 1 >= sg.ntiles;   // nothing to issue
-          bool pv_now = false;
+          // inputs): PV(t) goes out as soon as P(t) is ready, between QK
+          // chunks if need be, so a ring slot is released without waiting
+          // for the next tile's MMAs; polling uses the non-blocking
+          // mbarrier test (try_wait may sleep until its barrier flips).
+          int chunks = t + 1 < sg.ntiles ? 0 : kQkChunks;   // QK(t+1) chunks issued
+          bool pv = false;
           long long t_spin = 0;
-          while (!pv_now) {
-            // test_wait never suspends: a missing KV tile must not delay
-            // noticing P(t) (try_wait may sleep until its barrier flips)
-            if (!qk_next && mbar_test(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1)) {
+          while (!pv || chunks < kQkChunks) {
+            bool progressed = false;
+            if (!pv && mbar_test(&p_full[uc & 1], (uc >> 1) & 1)) {
               tc_fence_after();
-              issue_qk(kc + 1, uc + 1);
-              qk_next = true;
+              const uint32_t stage = smem_u32(sm_kv + (kc % kStages) * kStageBytes);
+#pragma unroll
+              for (int kk = 0; kk < kPvSteps; ++kk) {
+                // value half: boxes 4*half..4*half+3 (64 latent columns each),
+                // MN-major: N-blocks one box apart (LBO), 8-token groups SBO apart
+                const uint64_t bdesc = sdesc(stage + (4 * half) * kBox + kk * 2048, kBox,
+                                             G::kSBO, G::kSwizzle);
+                const uint32_t a = tmem + kColS + kTile * (uc & 1) + 8 * kk;
+                if (FP8) mma_f8_ts(tmem + kColO, a, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                else mma_f16_ts(tmem + kColO, a, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+              }
+              mma_commit(&kv_empty[kc % kStages]);
+              mma_commit(&pv_done[uc & 1]);
+              if (t + 1 == sg.ntiles) mma_commit(q_free);
+              pv = true;
+              progressed = true;
             }
-            if (mbar_test(&p_full[uc & 1], (uc >> 1) & 1)) {
-              pv_now = true;
-              break;
+            if (chunks < kQkChunks &&
+                (chunks > 0 || mbar_test(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1))) {
+              if (chunks == 0) tc_fence_after();
+              issue_qk_chunk(kc + 1, uc + 1, chunks);
+              ++chunks;
+              progressed = true;
             }
+            if (progressed) continue;
             if (*abort_flag) break;
             if (t_spin == 0) t_spin = clock64();
             else if (clock64() - t_spin > kWaitLimitCycles) { *abort_flag = 1; break; }
           }
-          if (!pv_now) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t stage = smem_u32(sm_kv + (kc % kStages) * kStageBytes);
-#pragma unroll
-          for (int kk = 0; kk < kPvSteps; ++kk) {
-            // value half: boxes 4*half..4*half+3 (64 latent columns each),
-            // MN-major: N-blocks one box apart (LBO), 8-token groups SBO apart
-            const uint64_t bdesc = sdesc(stage + (4 * half) * kBox + kk * 2048, kBox,
-                                         G::kSBO, G::kSwizzle);
-            const uint32_t a = tmem + kColS + kTile * (uc & 1) + 8 * kk;
-            if (FP8) mma_f8_ts(tmem + kColO, a, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-            else mma_f16_ts(tmem + kColO, a, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-          }
-          mma_commit(&kv_empty[kc % kStages]);
-          mma_commit(&pv_done[uc & 1]);
-          if (t + 1 == sg.ntiles) mma_commit(q_free);
-          if (!qk_next) {
-            ok = mbar_wait(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            issue_qk(kc + 1, uc + 1);
-          }
+          if (!pv || chunks < kQkChunks) { ok = false; break; }
         }
       }
       if (!ok) {
@@ -589,16 +613,26 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         const int pos0 = (sg.tile0 + t) * kTile;
         float x[kTile];
         float tmax = -INFINITY;
+        // interior tiles (every position inside [lo, hi)) skip the mask
+        const bool full_tile = pos0 >= sg.lo && pos0 + kTile <= sg.hi;
 #pragma unroll
         for (int c = 0; c < kTile; c += 32) {
           uint32_t sr[32];
           tmem_ld_x32(lane_base + kColS + kTile * sb + c, sr);
+          if (full_tile) {
 #pragma unroll
-          for (int jj = 0; jj < 32; ++jj) {
-            const int pos = pos0 + c + jj;
-            const bool valid = pos >= sg.lo && pos < sg.hi;
-            x[c + jj] = valid ? __uint_as_float(sr[jj]) * args.scale_log2 : -INFINITY;
-            tmax = fmaxf(tmax, x[c + jj]);
+            for (int jj = 0; jj < 32; ++jj) {
+              x[c + jj] = __uint_as_float(sr[jj]) * args.scale_log2;
+              tmax = fmaxf(tmax, x[c + jj]);
+            }
+          } else {
+#pragma unroll
+            for (int jj = 0; jj < 32; ++jj) {
+              const int pos = pos0 + c + jj;
+              const bool valid = pos >= sg.lo && pos < sg.hi;
+              x[c + jj] = valid ? __uint_as_float(sr[jj]) * args.scale_log2 : -INFINITY;
+              tmax = fmaxf(tmax, x[c + jj]);
+            }
           }
         }
         if (t > 0) {
@@ -613,7 +647,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
             ok = mbar_wait(&pv_done[up & 1], (up >> 1) & 1, abort_flag);
             if (!ok) break;
             tc_fence_after();
-            const float alpha = need ? exp2f(m - m_new) : 1.f;
+            const float alpha = need ? ex2(m - m_new) : 1.f;
 #pragma unroll 1
             for (int c = 0; c < 256; c += 32) {
               uint32_t o[32];
@@ -635,7 +669,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
         // P.V MMA actually consumes normalises O, so O stays a convex
         // combination of the value rows.
 #pragma unroll
-        for (int k = 0; k < kTile; ++k) x[k] = exp2f(x[k] - m);
+        for (int k = 0; k < kTile; ++k) x[k] = ex2(x[k] - m);
         float psum = 0.f, qsum = 0.f;
 #pragma unroll
         for (int k = 0; k < kTile; ++k) psum += x[k];

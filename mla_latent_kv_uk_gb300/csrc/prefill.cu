@@ -212,7 +212,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
           // more than one phase ahead of this wait (see the decode kernel)
           if (!(ok = mbar_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag))) break;
           tc_fence_after();
-          const float alpha = need ? (m == -INFINITY ? 0.f : exp2f(m - m_new)) : 1.f;
+          const float alpha = need ? (m == -INFINITY ? 0.f : ex2(m - m_new)) : 1.f;
 #pragma unroll 1
           for (int c = 0; c < kDv; c += 32) {
             uint32_t o[32];
@@ -236,7 +236,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const float p0 = exp2f(x[c + 2 * k] - ms), p1 = exp2f(x[c + 2 * k + 1] - ms);
+          const float p0 = ex2(x[c + 2 * k] - ms), p1 = ex2(x[c + 2 * k + 1] - ms);
           psum += p0 + p1;
           pk[k] = pack2(p0, p1);
         }

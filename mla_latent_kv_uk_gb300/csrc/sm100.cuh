@@ -129,6 +129,14 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
+// 2^x with the hardware approximation (MUFU.EX2; relative error ~2^-22,
+// flushes subnormal results to zero, ex2(-inf) = +0).
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // ------------------------------------------- programmatic dependent launch
 // Blocks until the preceding grid in the stream has completed and its
 // memory is visible (no-op when the launch did not opt into PDL).
