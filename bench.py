@@ -259,7 +259,8 @@ def run_ours(args, rank, world, device):
         "e2e": {"value": whole_job_rate(B, world, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": None,
+                     "frac": achieved / hbm, "traffic": DECODE_TRAFFIC,
+                     "traffic_source": DECODE_TRAFFIC_SOURCE,
                      "kernel": "mla_decode_paged (plan + decode + merge launches)",
                      "kernel_ms": ms_dec, "peak_source": src,
                      "tensor_tflops": flops / (ms_dec * 1e-3) / 1e12,
@@ -270,6 +271,14 @@ def run_ours(args, rank, world, device):
         "device_error": err,
     }
     return res
+
+
+# DRAM bytes (read + write) of one decode_kernel launch on this workload, from
+# the ncu capture summarised in profiles/decode_kernel_dsv3_b32_h128_ctx4096.md;
+# None whenever the kernel has changed since those counters were taken.
+DECODE_TRAFFIC = 164.37e6
+DECODE_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, decode_kernel, "
+                         "profiles/decode_kernel_dsv3_b32_h128_ctx4096.md (bytes per launch)")
 
 
 def oracle_sample(n_req):
