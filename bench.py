@@ -276,7 +276,7 @@ def run_ours(args, rank, world, device):
 # DRAM bytes (read + write) of one decode_kernel launch on this workload, from
 # the ncu capture summarised in profiles/decode_kernel_dsv3_b32_h128_ctx4096.md;
 # None whenever the kernel has changed since those counters were taken.
-DECODE_TRAFFIC = 164.37e6
+DECODE_TRAFFIC = None
 DECODE_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, decode_kernel, "
                          "profiles/decode_kernel_dsv3_b32_h128_ctx4096.md (bytes per launch)")
 

@@ -12,20 +12,18 @@
 // Design (GB300, sm_103a):
 //  * All 128 heads of a query token share one latent KV row, so per 64-token
 //    tile S = Q K^T is a dense [128 x 64 x 576] contraction and O += P V a
-//    [128 x 256 x 64] one: both run on tcgen05 with fp32 TMEM accumulators.
-//    A tcgen05.mma with M = 128, K = 16 costs about the same to issue for
-//    any N up to 128 (measured), so the tile is as wide in tokens as shared
-//    memory allows.
+//    [128 x 512 x 64] one: both run on tcgen05 with fp32 TMEM accumulators.
 //  * The fp32 output of 128 heads x 512 latent columns is exactly one SM's
-//    TMEM, so each work span is processed by a PAIR of CTAs: CTA c owns
-//    latent columns [256c, 256c + 256) of O and recomputes S itself (the
-//    two CTAs read the same KV tiles; the second read is an L2 hit).
-//  * TMEM (512 columns), bf16: O half [0,256), S/P double buffer [256,384),
-//    query dims 0..255 as the QK A operand [384,512); query dims 256..575
-//    stay in shared memory next to a 2-deep ring of 72 KB KV tiles.  e4m3:
-//    the whole query in shared memory, a 4-deep ring of 36 KB tiles.
-//  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer (+ TMEM owner),
-//    warps 2..5 online softmax (one head row per thread), correction and
+//    TMEM, so each work span is processed by a PAIR of CTAs, CTA c owning
+//    latent output columns [256c, 256c + 256).
+//  * bf16 (decode_pair_kernel): the pair is a 2-CTA cluster that splits the
+//    QK contraction by columns.  Each CTA loads only its latent half and its
+//    half of the rope columns of every KV tile, and the partial scores are
+//    summed through distributed shared memory (see the kernel's comment).
+//  * e4m3 (decode_kernel<true>): each CTA of the pair loads whole 36 KB
+//    tiles and recomputes S itself (the second read of a tile is an L2 hit).
+//  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer (+ TMEM owner), the
+//    other warps online softmax (one head row per thread), correction and
 //    epilogue.  Lazy rescaling: O is rescaled only when a row max grows by
 //    more than 2^8.
 //  * Work split (A3): every job (request, query token, 128-head group)
@@ -36,6 +34,7 @@
 #include <cuda_fp8.h>
 #include <math.h>
 
+#include <algorithm>
 #include <mutex>
 #include <type_traits>
 
@@ -59,19 +58,8 @@ template <bool FP8>
 struct Geo;
 
 template <>
-struct Geo<false> {                          // bf16 cache and query
-  static constexpr int kTile = 64;           // tokens per KV tile (= MMA N)
-  static constexpr int kStages = 2;
-  static constexpr int kRowBytes = 128;      // 64 bf16 per box row
-  static constexpr int kBox = kTile * kRowBytes;          // 8 KB
-  static constexpr int kStageBytes = 9 * kBox;            // 72 KB
-  static constexpr int kQBox = 128 * kRowBytes;           // 16 KB
-  static constexpr int kQsBoxes = 5;         // query dims 256..575 in smem
-  static constexpr int kQtCols = 128;        // query dims 0..255 in TMEM
-  static constexpr uint32_t kColQ = 384;
-  static constexpr int kKStep = 16;          // K per MMA instruction
-  static constexpr uint32_t kSwizzle = sm100::kSwizzle128B;
-  static constexpr uint32_t kSBO = 1024;     // 8 rows x 128 B
+struct Geo<false> {                          // bf16: only the tile width (the
+  static constexpr int kTile = 64;           // kernel geometry is `pair` below)
 };
 
 template <>
@@ -778,6 +766,623 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
   }
 }
 
+// ------------------------------------------------ bf16 split-QK pair kernel
+// The two CTAs of a 2-CTA cluster share one work span.  CTA c loads only
+// latent columns [256c, 256c + 256) of each KV tile plus rope columns
+// [32c, 32c + 32) (36 KB instead of 72 KB per tile) and computes the
+// partial scores of its 288 columns (16 latent K steps with the query in
+// TMEM, 2 rope K steps with the query rope half in shared memory).  The
+// partials are summed across the pair through distributed shared memory:
+//   * rows (heads) [64c, 64c + 64) are "own" rows of CTA c: it receives the
+//     peer's partial scores of those rows (16 KB bulk copy), runs the online
+//     softmax on them, writes the probabilities into its P operand tile and
+//     copies those rows, with the rescale factor and running row sum, into
+//     the peer's P operand tile;
+//   * the other 64 rows it forwards: it ships its partial scores to the peer
+//     and gets the probabilities back.
+// Each CTA still owns output columns [256c, 256c + 256) for all 128 heads,
+// and its value operand is exactly the latent boxes it loaded.  P lives in
+// shared memory (P.V reads it as the A operand), so a TMEM score buffer is
+// free as soon as both row groups have read it: QK runs up to two tiles
+// ahead of the softmax, independently of P.V, and the two message latencies
+// overlap other tiles' work instead of adding up per tile.
+namespace pair {
+constexpr int kTile = 64;
+constexpr int kStages = 4;
+constexpr int kBox = 8192;                      // 64 tokens x 64 bf16, SW128
+constexpr int kRopeBox = 4096;                  // 64 tokens x 32 bf16, SW64
+constexpr int kStageBytes = 4 * kBox + kRopeBox;   // 36 KB
+constexpr int kPBuf = 128 * 128;                // 128 heads x 64 tokens bf16, SW128
+constexpr int kQRopeBytes = 128 * 64;           // 128 heads x 32 rope dims, SW64
+constexpr int kSMsg = 64 * 64 * 4;              // 64 rows x 64 fp32 scores
+constexpr int kAlMsg = 2 * 64 * 4;              // alpha[64], lq[64]
+constexpr int kOffRing = 0;
+constexpr int kOffP = kOffRing + kStages * kStageBytes;       // [2] P operand tiles
+constexpr int kOffQ = kOffP + 2 * kPBuf;
+constexpr int kOffSSend = kOffQ + kQRopeBytes;
+constexpr int kOffSRecv = kOffSSend + kSMsg;
+constexpr int kOffAlSend = kOffSRecv + kSMsg;                 // [2]
+constexpr int kOffAlRecv = kOffAlSend + 2 * kAlMsg;           // [2]
+constexpr int kOffBars = kOffAlRecv + 2 * kAlMsg;
+constexpr int kNumBars = 2 * kStages + 18;
+constexpr int kSmem = kOffBars + kNumBars * 8 + 16 + 1024;
+constexpr int kQkChunks = 3;
+constexpr int kChunkSteps = 6;                  // 18 K=16 steps: 16 latent + 2 rope
+constexpr int kPvSteps = kTile / 16;
+constexpr uint32_t kColQ = 384;                 // query latent half, 128 columns
+constexpr uint32_t kPMsg = 64 * 128 + kAlMsg;   // bytes landing per P message
+static_assert(kSmem <= 232448, "shared memory of one CTA");
+static_assert(kOffP % 1024 == 0 && kOffQ % 1024 == 0 && kStageBytes % 1024 == 0,
+              "swizzled tiles start on 1024-byte boundaries");
+}  // namespace pair
+
+__global__ void __launch_bounds__(kThreads, 1)
+decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
+                   const __grid_constant__ CUtensorMap tm_kr,
+                   const __grid_constant__ CUtensorMap tm_qr, DecodeArgs args) {
+  using namespace pair;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sm_kv = smem + kOffRing;
+  uint8_t *sm_p = smem + kOffP;
+  uint8_t *sm_q = smem + kOffQ;
+  uint8_t *s_send = smem + kOffSSend;
+  uint8_t *s_recv = smem + kOffSRecv;
+  uint8_t *al_send = smem + kOffAlSend;
+  uint8_t *al_recv = smem + kOffAlRecv;
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
+  uint64_t *kv_full = bars;                 // [kStages]
+  uint64_t *kv_empty = bars + kStages;      // [kStages]
+  uint64_t *s_full = bars + 2 * kStages;    // [2] QK done
+  uint64_t *s_free = s_full + 2;            // [2] both row groups have read S
+  uint64_t *p_full = s_free + 2;            // [2] all 128 rows of P in place
+  uint64_t *pv_done = p_full + 2;           // [2]
+  uint64_t *xp_full = pv_done + 2;          // [2] the peer's P rows + factors landed
+  uint64_t *pb_free = xp_full + 2;          // [2] the peer's P.V of two tiles ago is done
+  uint64_t *q_full = pb_free + 2;
+  uint64_t *q_tmem = q_full + 1;
+  uint64_t *q_free = q_tmem + 1;
+  uint64_t *drain = q_free + 1;
+  uint64_t *xs_full = drain + 1;            // the peer's partial scores landed
+  uint64_t *xs_free = xs_full + 1;          // the peer consumed our last scores
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xs_free + 1);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int half = static_cast<int>(cluster_rank());
+  const uint32_t peer = static_cast<uint32_t>(half ^ 1);
+  const int group = blockIdx.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&kv_full[s], 1);
+      mbar_init(&kv_empty[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&s_full[s], 1);
+      mbar_init(&s_free[s], 4);     // lane 0 of each softmax warp
+      mbar_init(&p_full[s], 128);
+      mbar_init(&pv_done[s], 1);
+      mbar_init(&xp_full[s], 1);
+      mbar_init(&pb_free[s], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_tmem, 128);
+    mbar_init(q_free, 1);
+    mbar_init(drain, 1);
+    mbar_init(xs_full, 1);
+    mbar_init(xs_free, 2);          // lane 0 of each of the peer's own-row warps
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  // both CTAs' barriers exist before either sends the other anything
+  cluster_sync();
+  // the prologue above overlaps the plan kernel; the plan is read below
+  grid_dep_wait();
+  grid_dep_launch();
+
+  SegWalk walk;
+  walk.init(args.plan, args.J, args.q_len, args.H, args.HG, args.groups, group, kTile);
+  Seg sg;
+
+  if (warp == 0) {
+    // -------------------------------------------------- TMA producer
+    if (lane == 0) {
+      prefetch_tmap(&tm_kv);
+      prefetch_tmap(&tm_kr);
+      prefetch_tmap(&tm_qr);
+    }
+    int kc = 0, nseg = 0;
+    bool ok = true;
+    while (ok && walk.next(sg)) {
+      const int32_t *bt = args.block_table + static_cast<int64_t>(sg.b) * args.max_blocks;
+      int page_base = -(1 << 30), my_blk = -1;
+      auto blk_of = [&](int tile) -> int {  // warp-collective
+        const int page = tile * kTile / kPage;
+        if (page < page_base || page >= page_base + 32) {
+          page_base = page;
+          my_blk = page + lane < args.max_blocks ? __ldg(bt + page + lane) : -1;
+        }
+        return __shfl_sync(0xffffffffu, my_blk, page - page_base);
+      };
+      // Loads this CTA's part of KV tile `tile` into ring slot kc % kStages.
+      auto load_tile = [&](int tile) -> bool {
+        const int s = kc % kStages;
+        if (kc >= kStages && !mbar_wait(&kv_empty[s], ((kc / kStages) - 1) & 1, abort_flag))
+          return false;
+        const int blk = blk_of(tile);
+        if (lane == 0) {
+          int row;
+          if (blk < 0 || blk >= args.num_blocks) {
+            raise_error(args.err, MLA_DEVERR_BLOCK_ID);
+            row = args.num_blocks * kPage;  // out of range: TMA fills zeros
+          } else {
+            row = blk * kPage + (tile * kTile) % kPage;
+          }
+          uint8_t *dst = sm_kv + s * kStageBytes;
+          mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+          for (int j = 0; j < 4; ++j)
+            tma_load_2d(dst + j * kBox, &tm_kv, &kv_full[s], 256 * half + 64 * j, row);
+          tma_load_2d(dst + 4 * kBox, &tm_kr, &kv_full[s], kLatent + 32 * half, row);
+        }
+        ++kc;
+        return true;
+      };
+      const int pre = min(sg.ntiles, kStages);
+      for (int t = 0; ok && t < pre; ++t) ok = load_tile(sg.tile0 + t);
+      if (!ok) break;
+      if (nseg > 0 && !(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(q_full, kQRopeBytes);
+        tma_load_2d(sm_q, &tm_qr, q_full, kLatent + 32 * half, sg.row0);
+      }
+      ++nseg;
+      for (int t = pre; ok && t < sg.ntiles; ++t) ok = load_tile(sg.tile0 + t);
+    }
+    if (*abort_flag && lane == 0) {
+      volatile int no_abort = 0;
+      for (int k = max(0, kc - kStages); k < kc; ++k)
+        mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &no_abort);
+      if (nseg > 0) mbar_wait(q_full, (nseg - 1) & 1, &no_abort);
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------ MMA issuer
+      const uint32_t idesc_qk = idesc_bf16(128, kTile, false, false);
+      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      const uint32_t q_base = smem_u32(sm_q);
+      int kc = 0, uc = 0, nseg = 0;
+      bool ok = true;
+      // `chunk_c` is a std::integral_constant so the descriptor offsets are
+      // compile-time constants.
+      auto issue_qk_chunk_c = [&](int kcx, int ucx, auto chunk_c) {
+        constexpr int chunk = decltype(chunk_c)::value;
+        const uint32_t stage = smem_u32(sm_kv + (kcx % kStages) * kStageBytes);
+        const uint32_t d = tmem + kColS + kTile * (ucx & 1);
+#pragma unroll
+        for (int j = 0; j < kChunkSteps; ++j) {
+          const int k = chunk * kChunkSteps + j;
+          if (k < 16) {   // latent: A = query half in TMEM, B = own latent boxes
+            const uint64_t bdesc = sdesc(stage + (k / 4) * kBox + (k % 4) * 32, 16, 1024,
+                                         kSwizzle128B);
+            mma_f16_ts(d, tmem + kColQ + 8 * k, bdesc, idesc_qk, k > 0 ? 1u : 0u);
+          } else {        // rope: this CTA's 32 rope columns, two K steps
+            const int kk = k - 16;
+            const uint64_t bdesc = sdesc(stage + 4 * kBox + kk * 32, 16, 512, kSwizzle64B);
+            const uint64_t adesc = sdesc(q_base + kk * 32, 16, 512, kSwizzle64B);
+            mma_f16_ss(d, adesc, bdesc, idesc_qk, 1u);
+          }
+        }
+        if (chunk == kQkChunks - 1) mma_commit(&s_full[ucx & 1]);
+      };
+      auto issue_qk_chunk = [&](int kcx, int ucx, int chunk) {
+        static_assert(kQkChunks == 3, "dispatch below covers three chunks");
+        switch (chunk) {
+          case 0: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 0>{}); break;
+          case 1: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 1>{}); break;
+          default: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 2>{}); break;
+        }
+      };
+      // QK of global tile u may start once its KV tile has landed and both
+      // row groups have read the scores of tile u-2 out of the same buffer.
+      auto qk_ready = [&](int kcx, int ucx) -> bool {
+        return mbar_test(&kv_full[kcx % kStages], (kcx / kStages) & 1) &&
+               (ucx < 2 || mbar_test(&s_free[ucx & 1], ((ucx - 2) >> 1) & 1));
+      };
+      while (ok && walk.next(sg)) {
+        ok = mbar_wait(q_full, nseg & 1, abort_flag) &&
+             mbar_wait(q_tmem, nseg & 1, abort_flag);
+        if (!ok) break;
+        ++nseg;
+        // QK runs up to two tiles ahead of P.V (bounded by the two score
+        // buffers); P.V of tile t may go out between QK chunks.  `qn`
+        // counts this segment's tiles whose QK has been issued in full.
+        int qn = 0, qchunks = 0;
+        long long t_spin = 0;
+        for (int t = 0; t < sg.ntiles;) {
+          bool progressed = false;
+          if (qn < sg.ntiles && qn < t + 3 &&
+              (qchunks > 0 || qk_ready(kc + (qn - t), uc + (qn - t)))) {
+            if (qchunks == 0) tc_fence_after();
+            issue_qk_chunk(kc + (qn - t), uc + (qn - t), qchunks);
+            if (++qchunks == kQkChunks) { qchunks = 0; ++qn; }
+            progressed = true;
+          }
+          if (qn > t && mbar_test(&p_full[uc & 1], (uc >> 1) & 1)) {
+            tc_fence_after();
+            const uint32_t stage = smem_u32(sm_kv + (kc % kStages) * kStageBytes);
+            const uint32_t pbuf = smem_u32(sm_p + (uc & 1) * kPBuf);
+#pragma unroll
+            for (int kk = 0; kk < kPvSteps; ++kk) {
+              // A = P (K-major, 16 tokens per step); B = the four own latent
+              // boxes, MN-major: N-blocks one box apart (LBO), 8-token
+              // groups SBO apart
+              const uint64_t adesc = sdesc(pbuf + kk * 32, 16, 1024, kSwizzle128B);
+              const uint64_t bdesc = sdesc(stage + kk * 2048, kBox, 1024, kSwizzle128B);
+              mma_f16_ss(tmem + kColO, adesc, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+            }
+            mma_commit(&kv_empty[kc % kStages]);
+            mma_commit(&pv_done[uc & 1]);
+            if (t + 1 == sg.ntiles) mma_commit(q_free);
+            ++t; ++kc; ++uc;
+            progressed = true;
+          }
+          if (progressed) { t_spin = 0; continue; }
+          if (*abort_flag) { ok = false; break; }
+          if (t_spin == 0) t_spin = clock64();
+          else if (clock64() - t_spin > kWaitLimitCycles) { *abort_flag = 1; ok = false; break; }
+        }
+      }
+      if (!ok) {
+        mma_commit(drain);
+        volatile int no_abort = 0;
+        mbar_wait(drain, 0, &no_abort);
+      }
+    }
+  } else {
+    // ------------------------- softmax (own rows) / forwarding (peer rows)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;        // head row within the group
+    const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
+    const int tid = threadIdx.x - 64;         // 0..127
+    const bool own = (r >> 6) == half;
+    const int lr = r & 63;                    // row within a message
+    const bool leader = lr == 0;              // one thread per 64-thread group
+    const int wl = lr >> 5;                   // warp within the group
+    const uint32_t peer_s_recv = peer_smem(s_recv, peer);
+    const uint32_t peer_xs_full = peer_smem(xs_full, peer);
+    const uint32_t peer_xs_free = peer_smem(xs_free, peer);
+    int uc = 0;
+    bool ok = true;
+    // a timed-out wait ends the loop for the whole warp at once, so no
+    // warp-collective operation is left waiting for a lane that has gone
+    auto warp_ok = [](bool v) { return __all_sync(0xffffffffu, v); };
+    // Query latent dims [256*half, 256*half + 256) of row r -> TMEM columns
+    // [kColQ, kColQ + 128), two bf16 per 32-bit column.
+    auto load_q_tmem = [&](const Seg &seg) {
+      const uint4 *src = reinterpret_cast<const uint4 *>(
+                             args.q + static_cast<int64_t>(seg.row0 + r) * kDqk * 2) +
+                         32 * half;
+      const bool valid = r < seg.hrows;
+#pragma unroll 1
+      for (int c = 0; c < 2; ++c) {
+        uint32_t w[64];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          uint4 v = valid ? __ldg(src + c * 16 + k) : make_uint4(0, 0, 0, 0);
+          w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+        }
+        tmem_st_x32(lane_base + kColQ + 64 * c, w);
+        tmem_st_x32(lane_base + kColQ + 64 * c + 32, w + 32);
+      }
+      tc_fence_before();
+      mbar_arrive(q_tmem);
+    };
+    // Forwarded rows: partial scores of tile k (global count) -> the peer.
+    auto send_s = [&](int k) -> bool {
+      if (!warp_ok(mbar_wait(&s_full[k & 1], (k >> 1) & 1, abort_flag))) return false;
+      tc_fence_after();
+      uint32_t sv[kTile];
+      tmem_ld_x32(lane_base + kColS + kTile * (k & 1), sv);
+      tmem_ld_x32(lane_base + kColS + kTile * (k & 1) + 32, sv + 32);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[k & 1]);   // this warp's score rows are read
+      // the peer has consumed message k-1, so s_send and its s_recv are free
+      if (k > 0 && !warp_ok(mbar_wait(xs_free, (k - 1) & 1, abort_flag))) return false;
+      uint4 *dst = reinterpret_cast<uint4 *>(s_send + lr * 256);
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        dst[j ^ (lr & 15)] = make_uint4(sv[4 * j], sv[4 * j + 1], sv[4 * j + 2], sv[4 * j + 3]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      // this warp's 32 rows (8 KB, contiguous) -> the same place in the peer
+      if (lane == 0)
+        bulk_copy_to_peer(peer_s_recv + wl * (kSMsg / 2), s_send + wl * (kSMsg / 2), kSMsg / 2,
+                          peer_xs_full);
+      return true;
+    };
+    bool have = walk.next(sg);
+    if (have) load_q_tmem(sg);
+    float lq_in = 1.f;   // forwarded rows: the owner's running sum, last message
+    while (ok && have) {
+      float m = -INFINITY, l = 0.f, lq = 0.f;
+      const int len = __ldg(args.seq_lens + sg.b);
+      for (int t = 0; t < sg.ntiles; ++t, ++uc) {
+        const int sb = uc & 1;
+        uint8_t *pbuf = sm_p + sb * kPBuf;
+        if (own) {
+          // ---------------------------------------------- online softmax
+          ok = warp_ok(mbar_wait(&s_full[sb], (uc >> 1) & 1, abort_flag));
+          if (!ok) break;
+          tc_fence_after();
+          uint32_t sr[kTile];   // this CTA's partial scores of row r
+          tmem_ld_x32(lane_base + kColS + kTile * sb, sr);
+          tmem_ld_x32(lane_base + kColS + kTile * sb + 32, sr + 32);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&s_free[sb]);   // this warp's score rows are read
+          if (leader) mbar_arrive_expect_tx(xs_full, kSMsg);
+          ok = warp_ok(mbar_wait(xs_full, uc & 1, abort_flag));
+          if (!ok) break;
+          const int pos0 = (sg.tile0 + t) * kTile;
+          const bool full_tile = pos0 >= sg.lo && pos0 + kTile <= sg.hi;
+          const uint4 *src = reinterpret_cast<const uint4 *>(s_recv + lr * 256);
+          float x[kTile];   // full scores: (own partial + the peer's) * scale
+          float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+          // interior tiles (every position inside [lo, hi)) skip the mask
+          if (full_tile) {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const uint4 v = src[k ^ (lr & 15)];
+              const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                x[4 * k + e] =
+                    (__uint_as_float(sr[4 * k + e]) + __uint_as_float(pv[e])) * args.scale_log2;
+                mx[e] = fmaxf(mx[e], x[4 * k + e]);
+              }
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+              const uint4 v = src[k ^ (lr & 15)];
+              const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int pos = pos0 + 4 * k + e;
+                x[4 * k + e] =
+                    (pos >= sg.lo && pos < sg.hi)
+                        ? (__uint_as_float(sr[4 * k + e]) + __uint_as_float(pv[e])) * args.scale_log2
+                        : -INFINITY;
+                mx[e] = fmaxf(mx[e], x[4 * k + e]);
+              }
+            }
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive_remote(peer_xs_free);   // this warp's rows of s_recv are consumed
+          const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          float alpha = 1.f;
+          if (t > 0) {
+            const float m_new = fmaxf(m, tmax);
+            const bool need = m_new > m + kRescaleLog2;
+            if (__any_sync(0xffffffffu, need)) {
+              const int up = uc - 1;
+              ok = warp_ok(mbar_wait(&pv_done[up & 1], (up >> 1) & 1, abort_flag));
+              if (!ok) break;
+              tc_fence_after();
+              alpha = need ? ex2(m - m_new) : 1.f;
+#pragma unroll 1
+              for (int c = 0; c < 256; c += 32) {
+                uint32_t o[32];
+                tmem_ld_x32(lane_base + kColO + c, o);
+#pragma unroll
+                for (int k = 0; k < 32; ++k)
+                  o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                tmem_st_x32(lane_base + kColO + c, o);
+              }
+              l *= alpha;
+              lq *= alpha;
+              if (need) m = m_new;
+            }
+          } else {
+            m = tmax;
+          }
+          // four partial sums keep the dependency chains short
+          float ps[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int k = 0; k < kTile; ++k) {
+            x[k] = ex2(x[k] - m);
+            ps[k & 3] += x[k];
+          }
+          l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+          uint32_t pk[kTile / 2];
+#pragma unroll
+          for (int k = 0; k < kTile / 2; ++k) {
+            pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
+            qs[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+          }
+          lq += (qs[0] + qs[1]) + (qs[2] + qs[3]);
+          // P tile `sb` and the factor slot are free once P.V of tile uc-2
+          // is done here (and the copy out of them has landed) and in the
+          // peer (which takes our rows into its own P tile)
+          if (uc >= 2) {
+            const int up = uc - 2;
+            ok = warp_ok(mbar_wait(&pv_done[sb], (up >> 1) & 1, abort_flag) &&
+                         mbar_wait(&pb_free[sb], (up >> 1) & 1, abort_flag));
+            if (!ok) break;
+          }
+          // row r of the K-major, 128B-swizzled P operand: 8 chunks of 8 tokens
+          uint4 *prow = reinterpret_cast<uint4 *>(pbuf + r * 128);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            prow[j ^ (r & 7)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          // factors of this warp's rows: alpha[32] then lq[32]
+          float *al = reinterpret_cast<float *>(al_send + sb * kAlMsg + wl * (kAlMsg / 2));
+          al[lane] = alpha;
+          al[32 + lane] = lq;
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            // this warp's 32 rows of P (contiguous) and their factors -> the
+            // same places in the peer
+            const uint32_t xbar = peer_smem(&xp_full[sb], peer);
+            uint8_t *rows = pbuf + (64 * half + 32 * wl) * 128;
+            bulk_copy_to_peer(peer_smem(rows, peer), rows, 32 * 128, xbar);
+            uint8_t *al_dst = al_recv + sb * kAlMsg + wl * (kAlMsg / 2);
+            bulk_copy_to_peer(peer_smem(al_dst, peer), al, kAlMsg / 2, xbar);
+          }
+        } else {
+          // ------------------------------------------------ forwarding
+          // Our P.V of tile uc-2 is done: the peer may overwrite our P tile
+          // `sb` with its rows of tile uc.
+          if (leader && uc >= 2) {
+            const int up = uc - 2;
+            if (mbar_wait(&pv_done[sb], (up >> 1) & 1, abort_flag))
+              mbar_arrive_remote(peer_smem(&pb_free[sb], peer));
+          }
+          // The scores of the next tile of this segment go out as soon as
+          // QK has produced them, before or after the probabilities of this
+          // tile come back, whichever is possible first.  (Not across a
+          // segment end: the next segment's QK needs the query these
+          // threads stage after the segment's last tile.)
+          if (t == 0) ok = send_s(uc);
+          if (!ok) break;
+          if (leader) mbar_arrive_expect_tx(&xp_full[sb], kPMsg);
+          bool pending = t + 1 < sg.ntiles, got_p = false;
+          long long t_spin = 0;
+          while (pending || !got_p) {
+            bool progressed = false;
+            if (pending) {
+              const bool ready = mbar_test(&s_full[(uc + 1) & 1], ((uc + 1) >> 1) & 1) &&
+                                 mbar_test(xs_free, uc & 1);
+              if (__shfl_sync(0xffffffffu, ready, 0)) {
+                ok = send_s(uc + 1);
+                if (!ok) break;
+                pending = false;
+                progressed = true;
+              }
+            }
+            if (!got_p && __shfl_sync(0xffffffffu, mbar_test(&xp_full[sb], (uc >> 1) & 1), 0)) {
+              got_p = true;
+              progressed = true;
+            }
+            if (progressed) continue;
+            if (*abort_flag) { ok = false; break; }
+            if (t_spin == 0) t_spin = clock64();
+            else if (clock64() - t_spin > kWaitLimitCycles) { *abort_flag = 1; ok = false; break; }
+          }
+          ok = warp_ok(ok && mbar_wait(&xp_full[sb], (uc >> 1) & 1, abort_flag));
+          if (!ok) break;
+          // the peer's P rows are already in our P tile; apply its factors
+          const float *al =
+              reinterpret_cast<const float *>(al_recv + sb * kAlMsg + wl * (kAlMsg / 2));
+          const float alpha = al[lane];
+          lq_in = al[32 + lane];
+          if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+            const int up = uc - 1;
+            ok = warp_ok(mbar_wait(&pv_done[up & 1], (up >> 1) & 1, abort_flag));
+            if (!ok) break;
+            tc_fence_after();
+#pragma unroll 1
+            for (int c = 0; c < 256; c += 32) {
+              uint32_t o[32];
+              tmem_ld_x32(lane_base + kColO + c, o);
+#pragma unroll
+              for (int k = 0; k < 32; ++k)
+                o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+              tmem_st_x32(lane_base + kColO + c, o);
+            }
+          }
+        }
+        const int pos0 = (sg.tile0 + t) * kTile;
+        if (pos0 + kTile > len) {
+          // cache rows past seq_len may hold anything (even NaN bits): zero
+          // them in this CTA's value boxes so that P = 0 contributes nothing
+          const int first = max(0, len - pos0);
+          const int nrows = kTile - first;
+          uint8_t *vbase = sm_kv + (uc % kStages) * kStageBytes;
+          for (int idx = tid; idx < nrows * 4 * 8; idx += 128) {
+            const int box = idx / (nrows * 8);
+            const int rem = idx - box * nrows * 8;
+            reinterpret_cast<uint4 *>(vbase + box * kBox + (first + rem / 8) * 128)[rem % 8] =
+                make_uint4(0, 0, 0, 0);
+          }
+          fence_proxy_async_smem();
+        }
+        tc_fence_before();
+        mbar_arrive(&p_full[sb]);
+      }
+      if (!ok) break;
+      {
+        const int up = uc - 1;  // the last PV of this segment (all earlier ones are done too)
+        ok = warp_ok(mbar_wait(&pv_done[up & 1], (up >> 1) & 1, abort_flag));
+      }
+      if (!ok) break;
+      tc_fence_after();
+      const Seg cur = sg;
+      have = walk.next(sg);
+      if (have) load_q_tmem(sg);
+      // ---- epilogue: O / lq for this CTA's 256 latent columns, all rows
+      const float inv = args.out_scale / (own ? lq : lq_in);
+      const bool row_ok = r < cur.hrows;
+      const int64_t orow = static_cast<int64_t>(cur.out_row0 + r);
+#pragma unroll 1
+      for (int c = 0; c < 256; c += 32) {
+        uint32_t o[32];
+        tmem_ld_x32(lane_base + kColO + c, o);
+        if (!row_ok) continue;
+        float v[32];
+#pragma unroll
+        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
+        const int col = 256 * half + c;
+        if (cur.whole && args.out_dtype == MLA_BF16) {
+          uint4 *dst = reinterpret_cast<uint4 *>(
+              static_cast<__nv_bfloat16 *>(args.out) + orow * kLatent + col);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            dst[k] = make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]),
+                                pack_bf16(v[8 * k + 2], v[8 * k + 3]),
+                                pack_bf16(v[8 * k + 4], v[8 * k + 5]),
+                                pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+        } else {
+          float *base = cur.whole
+                            ? static_cast<float *>(args.out) + orow * kLatent + col
+                            : args.ws_o + (static_cast<int64_t>(cur.slot) * 128 + r) * kLatent + col;
+          float4 *dst = reinterpret_cast<float4 *>(base);
+#pragma unroll
+          for (int k = 0; k < 8; ++k)
+            dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+        }
+      }
+      if (row_ok && own) {
+        const float lse = (m + log2f(l)) * 0.69314718055994531f;
+        if (cur.whole) args.lse[orow] = lse;
+        else args.ws_lse[static_cast<int64_t>(cur.slot) * 128 + r] = lse;
+      }
+      tc_fence_before();
+    }
+  }
+  // every bulk copy this CTA issued has landed before either CTA leaves
+  bulk_wait_all();
+  __syncthreads();
+  cluster_sync();
+  if (threadIdx.x == 0 && *abort_flag) raise_error(args.err, MLA_DEVERR_TIMEOUT);
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // Combines the partials of every job cut into several spans; writes zeros
 // and -inf for jobs with an empty key range.  One warp per (job, head row).
 template <typename Tout>
@@ -826,9 +1431,53 @@ WsLayout ws_layout(int B, int q_len, int H, int max_seq_len, int split_tiles,
   return w;
 }
 
+// Launch configuration of the bf16 pair kernel: 2-CTA clusters, with
+// programmatic stream serialization after the plan kernel.
+struct PairLaunch {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[2];
+  PairLaunch(int clusters, cudaStream_t stream) {
+    cfg.gridDim = dim3(2 * clusters);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = pair::kSmem;
+    cfg.stream = stream;
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+  }
+};
+
+// Work groups (CTA pairs) per launch: one per two SMs, capped by how many
+// 2-CTA clusters of the pair kernel can be resident at once (a cluster
+// needs both SMs in one GPC), so the whole grid runs in a single wave.
+// Cached per device.
 int groups_for_device() {
+  constexpr int kMaxDevices = 64;
+  static int cache[kMaxDevices] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
   const int sms = device_sm_count();
-  return sms >= 2 ? sms / 2 : 1;
+  int g = sms >= 2 ? sms / 2 : 1;
+  if (dev < 0 || dev >= kMaxDevices) return g;
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[dev] > 0) return cache[dev];
+  int clusters = 0;
+  if (cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           pair::kSmem) == cudaSuccess) {
+    PairLaunch pl(g, nullptr);
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_pair_kernel, &pl.cfg) != cudaSuccess)
+      clusters = 0;
+  }
+  cudaGetLastError();   // a failed query leaves no sticky error behind
+  if (clusters > 0) g = std::min(g, clusters);
+  cache[dev] = g;
+  return g;
 }
 
 bool decode_shape_ok(int B, int q_len, int H) {
@@ -907,6 +1556,34 @@ int launch_decode(const void *q, const void *kv_cache, int B, int q_len, int H,
   return MLA_OK;
 }
 
+int launch_decode_pair(const void *q, const void *kv_cache, int B, int q_len, int H,
+                       int num_blocks, DecodeArgs a, mla_stream_t stream) {
+  // KV latent boxes {64 columns, 64 tokens} (128B swizzle); KV and query
+  // rope halves {32 columns, 64 tokens / 128 heads} (64B swizzle)
+  CUtensorMap tm_kv, tm_kr, tm_qr;
+  const uint64_t row_bytes = static_cast<uint64_t>(kDqk) * 2;
+  const uint64_t kv_dims[2] = {kDqk, static_cast<uint64_t>(num_blocks) * kPage};
+  const uint64_t q_dims[2] = {kDqk, static_cast<uint64_t>(B) * q_len * H};
+  const uint64_t strides[1] = {row_bytes};
+  const uint32_t box_kv[2] = {64, static_cast<uint32_t>(pair::kTile)};
+  const uint32_t box_kr[2] = {32, static_cast<uint32_t>(pair::kTile)};
+  const uint32_t box_qr[2] = {32, 128};
+  if (!make_tmap(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, kv_dims, strides, box_kv,
+                 CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, kv_dims, strides, box_kr,
+                 CU_TENSOR_MAP_SWIZZLE_64B) ||
+      !make_tmap(&tm_qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, q_dims, strides, box_qr,
+                 CU_TENSOR_MAP_SWIZZLE_64B))
+    return MLA_ERR_CUDA;
+  if (cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           pair::kSmem) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  PairLaunch pl(a.groups, stream);
+  if (cudaLaunchKernelEx(&pl.cfg, decode_pair_kernel, tm_kv, tm_kr, tm_qr, a) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
+}
+
 }  // namespace
 
 extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
@@ -976,7 +1653,7 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   a.ws_lse = ws_lse;
   a.err = err;
   const int st = fp8 ? launch_decode<true>(q, kv_cache, B, q_len, H, num_blocks, a, stream)
-                     : launch_decode<false>(q, kv_cache, B, q_len, H, num_blocks, a, stream);
+                     : launch_decode_pair(q, kv_cache, B, q_len, H, num_blocks, a, stream);
   if (st != MLA_OK) return st;
 
   const int64_t rows = static_cast<int64_t>(J) * 128;
