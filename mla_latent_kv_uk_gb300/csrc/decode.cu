@@ -1332,38 +1332,67 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       const Seg cur = sg;
       have = walk.next(sg);
       if (have) load_q_tmem(sg);
-      // ---- epilogue: O / lq for this CTA's 256 latent columns, all rows
+      // ---- epilogue: O / lq for this CTA's 256 latent columns, all rows.
+      // Each warp stages 32 rows x 32 columns at a time in its 4 KB slice of
+      // the P tiles (idle now: P.V of this segment is done and the peer
+      // sends the next segment's P only after our signal for it), so every
+      // store instruction writes whole row segments instead of one 16-byte
+      // piece of 32 different rows.
       const float inv = args.out_scale / (own ? lq : lq_in);
       const bool row_ok = r < cur.hrows;
-      const int64_t orow = static_cast<int64_t>(cur.out_row0 + r);
+      const bool bf16_out = cur.whole && args.out_dtype == MLA_BF16;
+      uint4 *stage = reinterpret_cast<uint4 *>(sm_p + (warp - 2) * 4096);
 #pragma unroll 1
       for (int c = 0; c < 256; c += 32) {
         uint32_t o[32];
         tmem_ld_x32(lane_base + kColO + c, o);
-        if (!row_ok) continue;
         float v[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
-        const int col = 256 * half + c;
-        if (cur.whole && args.out_dtype == MLA_BF16) {
-          uint4 *dst = reinterpret_cast<uint4 *>(
-              static_cast<__nv_bfloat16 *>(args.out) + orow * kLatent + col);
+        if (bf16_out) {
+          // row = 64 bytes = 4 chunks of 8 bf16
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            dst[k] = make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]),
-                                pack_bf16(v[8 * k + 2], v[8 * k + 3]),
-                                pack_bf16(v[8 * k + 4], v[8 * k + 5]),
-                                pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+            stage[lane * 4 + (k ^ (lane & 3))] =
+                make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]), pack_bf16(v[8 * k + 2], v[8 * k + 3]),
+                           pack_bf16(v[8 * k + 4], v[8 * k + 5]), pack_bf16(v[8 * k + 6], v[8 * k + 7]));
         } else {
-          float *base = cur.whole
-                            ? static_cast<float *>(args.out) + orow * kLatent + col
-                            : args.ws_o + (static_cast<int64_t>(cur.slot) * 128 + r) * kLatent + col;
-          float4 *dst = reinterpret_cast<float4 *>(base);
+          // row = 128 bytes = 8 chunks of 4 fp32
 #pragma unroll
           for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+            stage[lane * 8 + (k ^ (lane & 7))] =
+                make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
+                           __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
         }
+        __syncwarp();
+        const int col = 256 * half + c;
+        if (bf16_out) {
+#pragma unroll
+          for (int it = 0; it < 4; ++it) {
+            const int row = it * 8 + (lane >> 2), ch = lane & 3;   // 8 rows per instruction
+            const int R = quarter * 32 + row;
+            if (R < cur.hrows)
+              reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.out) +
+                                        static_cast<int64_t>(cur.out_row0 + R) * kLatent + col)[ch] =
+                  stage[row * 4 + (ch ^ (row & 3))];
+          }
+        } else {
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int row = it * 4 + (lane >> 3), ch = lane & 7;   // 4 rows per instruction
+            const int R = quarter * 32 + row;
+            if (R < cur.hrows) {
+              float *base = cur.whole
+                                ? static_cast<float *>(args.out) +
+                                      static_cast<int64_t>(cur.out_row0 + R) * kLatent + col
+                                : args.ws_o + (static_cast<int64_t>(cur.slot) * 128 + R) * kLatent + col;
+              reinterpret_cast<uint4 *>(base)[ch] = stage[row * 8 + (ch ^ (row & 7))];
+            }
+          }
+        }
+        __syncwarp();
       }
+      const int64_t orow = static_cast<int64_t>(cur.out_row0 + r);
       if (row_ok && own) {
         const float lse = (m + log2f(l)) * 0.69314718055994531f;
         if (cur.whole) args.lse[orow] = lse;
