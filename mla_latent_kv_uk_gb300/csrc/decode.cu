@@ -204,6 +204,7 @@ struct Seg {
   int lo, hi;           // key range
   int tile0, ntiles;    // first absolute tile, tiles in this segment
   int whole, slot;      // covers the whole job?  partial slot otherwise
+  int len;              // seq_len of the request (set by the pair kernel's producer)
 };
 
 struct SegWalk {
@@ -804,8 +805,10 @@ constexpr int kOffSRecv = kOffSSend + kSMsg;
 constexpr int kOffAlSend = kOffSRecv + kSMsg;                 // [2]
 constexpr int kOffAlRecv = kOffAlSend + 2 * kAlMsg;           // [2]
 constexpr int kOffBars = kOffAlRecv + 2 * kAlMsg;
-constexpr int kNumBars = 2 * kStages + 18;
-constexpr int kSmem = kOffBars + kNumBars * 8 + 16 + 1024;
+constexpr int kNumBars = 2 * kStages + 27;
+constexpr int kSegSlots = 4;                    // segment descriptors in flight
+constexpr int kOffSegQ = kOffBars + kNumBars * 8 + 16;
+constexpr int kSmem = kOffSegQ + kSegSlots * 64 + 1024;
 constexpr int kQkChunks = 3;
 constexpr int kChunkSteps = 6;                  // 18 K=16 steps: 16 latent + 2 rope
 constexpr int kPvSteps = kTile / 16;
@@ -846,7 +849,12 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
   uint64_t *drain = q_free + 1;
   uint64_t *xs_full = drain + 1;            // the peer's partial scores landed
   uint64_t *xs_free = xs_full + 1;          // the peer consumed our last scores
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(xs_free + 1);
+  uint64_t *seg_full = xs_free + 1;         // [kSegSlots] descriptor published
+  uint64_t *seg_empty = seg_full + kSegSlots;   // [kSegSlots] every consumer has copied it
+  uint64_t *stage_ok = seg_empty + kSegSlots;   // outgoing copies have read the P tiles
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(stage_ok + 1);
+  Seg *segq = reinterpret_cast<Seg *>(smem + kOffSegQ);   // [kSegSlots]
+  static_assert(sizeof(Seg) <= 64, "segment descriptor slot");
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
 
   const int warp = warp_id(), lane = lane_id();
@@ -873,6 +881,11 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     mbar_init(drain, 1);
     mbar_init(xs_full, 1);
     mbar_init(xs_free, 2);          // lane 0 of each of the peer's own-row warps
+    for (int s = 0; s < kSegSlots; ++s) {
+      mbar_init(&seg_full[s], 1);
+      mbar_init(&seg_empty[s], 5);  // the MMA thread and lane 0 of each softmax warp
+    }
+    mbar_init(stage_ok, 4);         // lane 0 of each softmax warp, once per segment
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -903,7 +916,26 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     }
     int kc = 0, nseg = 0;
     bool ok = true;
+    // Publishes segment descriptor `ns` (or the end marker, ntiles = -1) in
+    // the shared-memory ring read by the MMA thread and the softmax warps,
+    // so they never walk the plan in global memory themselves.
+    auto publish = [&](int ns, bool end) -> bool {
+      const int slot = ns % kSegSlots;
+      if (ns >= kSegSlots &&
+          !mbar_wait(&seg_empty[slot], ((ns / kSegSlots) - 1) & 1, abort_flag))
+        return false;
+      if (lane == 0) {
+        Seg d = sg;
+        if (end) d.ntiles = -1;
+        segq[slot] = d;
+        mbar_arrive(&seg_full[slot]);
+      }
+      __syncwarp();
+      return true;
+    };
     while (ok && walk.next(sg)) {
+      sg.len = __ldg(args.seq_lens + sg.b);
+      if (!(ok = publish(nseg, false))) break;
       const int32_t *bt = args.block_table + static_cast<int64_t>(sg.b) * args.max_blocks;
       int page_base = -(1 << 30), my_blk = -1;
       auto blk_of = [&](int tile) -> int {  // warp-collective
@@ -948,6 +980,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       ++nseg;
       for (int t = pre; ok && t < sg.ntiles; ++t) ok = load_tile(sg.tile0 + t);
     }
+    if (ok) publish(nseg, true);
     if (*abort_flag && lane == 0) {
       volatile int no_abort = 0;
       for (int k = max(0, kc - kStages); k < kc; ++k)
@@ -998,7 +1031,15 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
         return mbar_test(&kv_full[kcx % kStages], (kcx / kStages) & 1) &&
                (ucx < 2 || mbar_test(&s_free[ucx & 1], ((ucx - 2) >> 1) & 1));
       };
-      while (ok && walk.next(sg)) {
+      while (ok) {
+        // segment nseg from the producer's queue
+        {
+          const int slot = nseg % kSegSlots;
+          if (!(ok = mbar_wait(&seg_full[slot], (nseg / kSegSlots) & 1, abort_flag))) break;
+          sg = segq[slot];
+          mbar_arrive(&seg_empty[slot]);
+          if (sg.ntiles < 0) break;
+        }
         ok = mbar_wait(q_full, nseg & 1, abort_flag) &&
              mbar_wait(q_tmem, nseg & 1, abort_flag);
         if (!ok) break;
@@ -1111,12 +1152,29 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                           peer_xs_full);
       return true;
     };
-    bool have = walk.next(sg);
+    // Takes the next segment descriptor from the producer's queue
+    // (warp-wide); false at the end marker or on a timeout (then ok = false).
+    int ns = 0;
+    auto take_seg = [&](Seg &out) -> bool {
+      const int slot = ns % kSegSlots;
+      if (!warp_ok(mbar_wait(&seg_full[slot], (ns / kSegSlots) & 1, abort_flag))) {
+        ok = false;
+        return false;
+      }
+      out = segq[slot];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&seg_empty[slot]);
+      ++ns;
+      return out.ntiles >= 0;
+    };
+    bool have = take_seg(sg);
     if (have) load_q_tmem(sg);
+    Seg nxt;
+    bool have_next = false;
     float lq_in = 1.f;   // forwarded rows: the owner's running sum, last message
     while (ok && have) {
       float m = -INFINITY, l = 0.f, lq = 0.f;
-      const int len = __ldg(args.seq_lens + sg.b);
+      const int len = sg.len;
       for (int t = 0; t < sg.ntiles; ++t, ++uc) {
         const int sb = uc & 1;
         uint8_t *pbuf = sm_p + sb * kPBuf;
@@ -1321,6 +1379,14 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
         }
         tc_fence_before();
         mbar_arrive(&p_full[sb]);
+        if (t + 1 == sg.ntiles) {
+          // QK of this segment is complete (this thread has waited for the
+          // last tile's scores), so the next segment's query can go into
+          // TMEM now, overlapping the last P.V and the exchange with the peer
+          have_next = take_seg(nxt);
+          if (!ok) break;
+          if (have_next) load_q_tmem(nxt);
+        }
       }
       if (!ok) break;
       {
@@ -1329,9 +1395,17 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       }
       if (!ok) break;
       tc_fence_after();
+      // The epilogue stages through P tile 0: every bulk copy out of the P
+      // tiles (this CTA's rows of P to the peer) must have been read first.
+      if (lane == 0) {
+        bulk_wait_read_all();
+        mbar_arrive(stage_ok);
+      }
+      ok = warp_ok(mbar_wait(stage_ok, (ns - 2) & 1, abort_flag));   // segment ns-2
+      if (!ok) break;
       const Seg cur = sg;
-      have = walk.next(sg);
-      if (have) load_q_tmem(sg);
+      sg = nxt;
+      have = have_next;
       // ---- epilogue: O / lq for this CTA's 256 latent columns, all rows.
       // Each warp stages 32 rows x 32 columns at a time in its 4 KB slice of
       // the P tiles (idle now: P.V of this segment is done and the peer

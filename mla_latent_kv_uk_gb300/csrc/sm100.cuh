@@ -394,6 +394,12 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, const vo
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
+// Waits until every bulk copy this thread committed has finished reading
+// its source (the source may be overwritten afterwards).
+__device__ __forceinline__ void bulk_wait_read_all() {
+  asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Waits until every bulk copy this thread committed has completed.
 __device__ __forceinline__ void bulk_wait_all() {
   asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");

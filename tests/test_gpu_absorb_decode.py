@@ -273,6 +273,21 @@ def test_decode_config5_sampled(m):
     _check(out[pick], lse[pick], ro, rl)
 
 
+def test_decode_reruns_bit_identical(m):
+    """Race check: the split-KV work assignment is fixed, so repeated runs
+    must agree bit for bit.  The spec-decode shape (many jobs, spans that
+    cross job boundaries, partial merges) exercises every hand-off of the
+    paired-CTA kernel; a hand-off that is not ordered shows up as a rerun
+    that differs (this is how a staging-buffer race was caught)."""
+    case = synth.config5_decode()
+    out0, lse0 = _run_decode(m, case)
+    ob0, lb0 = bits(out0), bits(lse0)
+    for _ in range(40):
+        out, lse = _run_decode(m, case)
+        assert np.array_equal(bits(out), ob0)
+        assert np.array_equal(bits(lse), lb0)
+
+
 # ------------------------------------------------------------- fp8 decode
 FP8_OUT_TOL, FP8_LSE_TOL = 5e-2, 1e-2
 
