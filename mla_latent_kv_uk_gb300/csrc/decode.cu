@@ -1503,7 +1503,7 @@ decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
   const int s0 = sp[j], nseg = sp[j + 1] - s0;
   if (nseg == 1) return;  // written directly by the decode kernel
   const int64_t orow = static_cast<int64_t>(j / HG) * H + hg * 128 + r;
-  merge_row<float, Tout>(ws_o + (static_cast<int64_t>(s0) * 128 + r) * kLatent,
+  merge_row<float, Tout, 2>(ws_o + (static_cast<int64_t>(s0) * 128 + r) * kLatent,
                          static_cast<int64_t>(128) * kLatent,
                          ws_lse + static_cast<int64_t>(s0) * 128 + r, 128, nseg,
                          kLatent, out + orow * kLatent, lse + orow,

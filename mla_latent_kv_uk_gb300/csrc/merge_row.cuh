@@ -44,8 +44,14 @@ __device__ __forceinline__ void store8(float *p, const float *v) {
 }
 
 // part s of the row lives at part0 + s * part_stride (elements); its LSE at
-// lse0[s * lse_stride].  D % 8 == 0, D <= 1024.
-template <typename Tin, typename Tout>
+// lse0[s * lse_stride].  D % 8 == 0, D <= 256 * NC (NC 16-byte chunk slots
+// per lane).
+//
+// Latency layout: lane s holds the LSE of part s (32 parts per pass), the
+// weights come from shuffles, and the row data of up to four parts is
+// requested before any of it is used, so a row costs a few L2 round trips
+// instead of two per part.
+template <typename Tin, typename Tout, int NC = 4>
 __device__ __forceinline__ void merge_row(const Tin *part0, int64_t part_stride,
                                           const float *lse0, int64_t lse_stride,
                                           int S, int D, Tout *out,
@@ -61,32 +67,53 @@ __device__ __forceinline__ void merge_row(const Tin *part0, int64_t part_stride,
     if (out_lse && lane == 0) *out_lse = -INFINITY;
     return;
   }
-  float acc[4][8];
+  float acc[NC][8];
 #pragma unroll
-  for (int i = 0; i < 4; ++i)
+  for (int i = 0; i < NC; ++i)
 #pragma unroll
     for (int e = 0; e < 8; ++e) acc[i][e] = 0.f;
   float z = 0.f;
-  for (int s = 0; s < S; ++s) {
-    const float l = lse0[s * lse_stride];
-    if (l == -INFINITY) continue;
-    const float w = expf(l - m);
-    z += w;
-    const Tin *p = part0 + s * part_stride;
+  for (int s0 = 0; s0 < S; s0 += 32) {
+    // this pass's weights: lane k holds part s0 + k's (0 for -inf or absent)
+    const int sk = s0 + lane;
+    const float lk = sk < S ? lse0[sk * lse_stride] : -INFINITY;
+    const float wk = lk == -INFINITY ? 0.f : expf(lk - m);
+    float zk = wk;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = lane + 32 * i;
-      if (c < chunks) {
-        float v[8];
-        load8(p + c * 8, v);
+    for (int o = 16; o; o >>= 1) zk += __shfl_xor_sync(0xffffffffu, zk, o);
+    z += zk;
+    const int n = min(32, S - s0);
+    for (int b = 0; b < n; b += 4) {
+      float w[4];
+      float v[4][NC][8];   // [part][chunk slot][element]
 #pragma unroll
-        for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(w, v[e], acc[i][e]);
+      for (int u = 0; u < 4; ++u) {
+        w[u] = __shfl_sync(0xffffffffu, wk, (b + u) & 31);
+        const bool use = b + u < n && w[u] != 0.f;   // weight-0 parts are never read
+        const Tin *p = part0 + static_cast<int64_t>(s0 + b + u) * part_stride;
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+          const int c = lane + 32 * i;
+          if (use && c < chunks) load8(p + c * 8, v[u][i]);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        if (!(b + u < n && w[u] != 0.f)) continue;
+#pragma unroll
+        for (int i = 0; i < NC; ++i) {
+          const int c = lane + 32 * i;
+          if (c < chunks) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[i][e] = fmaf(w[u], v[u][i][e], acc[i][e]);
+          }
+        }
       }
     }
   }
   const float inv = 1.f / z;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) {
+  for (int i = 0; i < NC; ++i) {
     const int c = lane + 32 * i;
     if (c < chunks) {
       float v[8];
