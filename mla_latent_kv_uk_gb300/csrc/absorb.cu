@@ -111,6 +111,10 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched with programmatic stream serialization: the prologue above
+  // overlaps the previous kernel; every global read comes after this wait
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_w);
@@ -248,6 +252,10 @@ vup_kernel(const __grid_constant__ CUtensorMap tm_w,
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // launched with programmatic stream serialization: the prologue above
+  // overlaps the previous kernel; every global read comes after this wait
+  grid_dep_wait();
+  grid_dep_launch();
 
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_w);
@@ -371,8 +379,9 @@ extern "C" int mla_absorb_q(const void *q_nope, const void *q_pe,
                            static_cast<int>(smem)) != cudaSuccess)
     return MLA_ERR_CUDA;
   dim3 grid(2, H, (T + NT - 1) / NT);
-  absorb_kernel<<<grid, kThreads, smem, stream>>>(ta, tb, a);
-  return launch_status();
+  if (launch_pdl(absorb_kernel, grid, dim3(kThreads), smem, stream, ta, tb, a) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 extern "C" int mla_v_up(const void *o_lat, const void *w_uv, int T, int H,
@@ -413,6 +422,7 @@ extern "C" int mla_v_up(const void *o_lat, const void *w_uv, int T, int H,
                            static_cast<int>(smem)) != cudaSuccess)
     return MLA_ERR_CUDA;
   dim3 grid(H, (T + NT - 1) / NT);
-  vup_kernel<<<grid, kThreads, smem, stream>>>(ta, tb, a, stages);
-  return launch_status();
+  if (launch_pdl(vup_kernel, grid, dim3(kThreads), smem, stream, ta, tb, a, stages) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }

@@ -1195,40 +1195,36 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           const int pos0 = (sg.tile0 + t) * kTile;
           const bool full_tile = pos0 >= sg.lo && pos0 + kTile <= sg.hi;
           const uint4 *src = reinterpret_cast<const uint4 *>(s_recv + lr * 256);
-          float x[kTile];   // full scores: (own partial + the peer's) * scale
+          // Full scores s = own partial + the peer's (paired adds); the tile
+          // max is taken on s and scaled once (exact: scaling by a positive
+          // constant keeps the order and rounds each product alike), and
+          // the exponent s * scale - m is one paired FMA below.
+          float x[kTile];
           float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            const uint4 v = src[k ^ (lr & 15)];
+            add_f32x2(x[4 * k], x[4 * k + 1], __uint_as_float(sr[4 * k]),
+                      __uint_as_float(sr[4 * k + 1]), __uint_as_float(v.x), __uint_as_float(v.y));
+            add_f32x2(x[4 * k + 2], x[4 * k + 3], __uint_as_float(sr[4 * k + 2]),
+                      __uint_as_float(sr[4 * k + 3]), __uint_as_float(v.z), __uint_as_float(v.w));
+          }
           // interior tiles (every position inside [lo, hi)) skip the mask
           if (full_tile) {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const uint4 v = src[k ^ (lr & 15)];
-              const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                x[4 * k + e] =
-                    (__uint_as_float(sr[4 * k + e]) + __uint_as_float(pv[e])) * args.scale_log2;
-                mx[e] = fmaxf(mx[e], x[4 * k + e]);
-              }
-            }
+            for (int k = 0; k < kTile; ++k) mx[k & 3] = fmaxf(mx[k & 3], x[k]);
           } else {
 #pragma unroll
-            for (int k = 0; k < 16; ++k) {
-              const uint4 v = src[k ^ (lr & 15)];
-              const uint32_t pv[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int pos = pos0 + 4 * k + e;
-                x[4 * k + e] =
-                    (pos >= sg.lo && pos < sg.hi)
-                        ? (__uint_as_float(sr[4 * k + e]) + __uint_as_float(pv[e])) * args.scale_log2
-                        : -INFINITY;
-                mx[e] = fmaxf(mx[e], x[4 * k + e]);
-              }
+            for (int k = 0; k < kTile; ++k) {
+              const int pos = pos0 + k;
+              x[k] = (pos >= sg.lo && pos < sg.hi) ? x[k] : -INFINITY;
+              mx[k & 3] = fmaxf(mx[k & 3], x[k]);
             }
           }
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(peer_xs_free);   // this warp's rows of s_recv are consumed
-          const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+          const float tmax =
+              fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * args.scale_log2;
           float alpha = 1.f;
           if (t > 0) {
             const float m_new = fmaxf(m, tmax);
@@ -1255,19 +1251,30 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           } else {
             m = tmax;
           }
-          // four partial sums keep the dependency chains short
+          // p = 2^(s * scale - m): paired FMAs, then the hardware ex2; the
+          // row sums accumulate in pairs (four chains)
+          const float nm = -m, sc = args.scale_log2;
+#pragma unroll
+          for (int k = 0; k < kTile; k += 2)
+            fma_f32x2(x[k], x[k + 1], x[k], x[k + 1], sc, sc, nm, nm);
+#pragma unroll
+          for (int k = 0; k < kTile; ++k) x[k] = ex2(x[k]);
           float ps[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int k = 0; k < kTile; ++k) {
-            x[k] = ex2(x[k] - m);
-            ps[k & 3] += x[k];
+          for (int k = 0; k < kTile; k += 4) {
+            add_f32x2(ps[0], ps[1], ps[0], ps[1], x[k], x[k + 1]);
+            add_f32x2(ps[2], ps[3], ps[2], ps[3], x[k + 2], x[k + 3]);
           }
           l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
           uint32_t pk[kTile / 2];
 #pragma unroll
-          for (int k = 0; k < kTile / 2; ++k) {
-            pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
-            qs[k & 3] += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
+          for (int k = 0; k < kTile / 2; ++k) pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
+#pragma unroll
+          for (int k = 0; k < kTile / 2; k += 2) {
+            add_f32x2(qs[0], qs[1], qs[0], qs[1], __uint_as_float(pk[k] << 16),
+                      __uint_as_float(pk[k] & 0xFFFF0000u));
+            add_f32x2(qs[2], qs[3], qs[2], qs[3], __uint_as_float(pk[k + 1] << 16),
+                      __uint_as_float(pk[k + 1] & 0xFFFF0000u));
           }
           lq += (qs[0] + qs[1]) + (qs[2] + qs[3]);
           // P tile `sb` and the factor slot are free once P.V of tile uc-2
@@ -1494,6 +1501,7 @@ decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
                     const float *__restrict__ ws_o,
                     const float *__restrict__ ws_lse, Tout *out, float *lse) {
   sm100::grid_dep_wait();   // partials of the decode grid
+  sm100::grid_dep_launch();
   const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
   const int j = row >> 7, r = row & 127;
   if (j >= J) return;
