@@ -276,9 +276,11 @@ def run_ours(args, rank, world, device):
 # DRAM bytes (read + write) of one decode_kernel launch on this workload, from
 # the ncu capture summarised in profiles/decode_pair_kernel_dsv3_b32_h128_ctx4096.md;
 # None whenever the kernel has changed since those counters were taken.
-DECODE_TRAFFIC = 164.17e6
-DECODE_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, decode_pair_kernel, "
-                         "profiles/decode_pair_kernel_dsv3_b32_h128_ctx4096.md (bytes per launch)")
+# DRAM bytes per launch of the decode kernel from an ncu capture; None while
+# the kernel has changed since the last capture.
+DECODE_TRAFFIC = None
+DECODE_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, decode_pair_kernel: "
+                         "not re-captured since the kernel last changed")
 
 
 def oracle_sample(n_req):

@@ -283,9 +283,7 @@ struct DecodeArgs {
 };
 
 __device__ __forceinline__ uint32_t pack_bf16(float a, float b) {
-  const uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(a));
-  const uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(b));
-  return lo | (hi << 16);
+  return bf16x2_rn(a, b);
 }
 
 // Four probabilities -> four e4m3 codes in one 32-bit TMEM column (element
@@ -805,7 +803,7 @@ constexpr int kOffSRecv = kOffSSend + kSMsg;
 constexpr int kOffAlSend = kOffSRecv + kSMsg;                 // [2]
 constexpr int kOffAlRecv = kOffAlSend + 2 * kAlMsg;           // [2]
 constexpr int kOffBars = kOffAlRecv + 2 * kAlMsg;
-constexpr int kNumBars = 2 * kStages + 27;
+constexpr int kNumBars = 2 * kStages + 28;
 constexpr int kSegSlots = 4;                    // segment descriptors in flight
 constexpr int kOffSegQ = kOffBars + kNumBars * 8 + 16;
 constexpr int kSmem = kOffSegQ + kSegSlots * 64 + 1024;
@@ -822,7 +820,9 @@ static_assert(kOffP % 1024 == 0 && kOffQ % 1024 == 0 && kStageBytes % 1024 == 0,
 __global__ void __launch_bounds__(kThreads, 1)
 decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                    const __grid_constant__ CUtensorMap tm_kr,
-                   const __grid_constant__ CUtensorMap tm_qr, DecodeArgs args) {
+                   const __grid_constant__ CUtensorMap tm_qr,
+                   const __grid_constant__ CUtensorMap tm_out,
+                   const __grid_constant__ CUtensorMap tm_ws, DecodeArgs args) {
   using namespace pair;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -852,7 +852,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
   uint64_t *seg_full = xs_free + 1;         // [kSegSlots] descriptor published
   uint64_t *seg_empty = seg_full + kSegSlots;   // [kSegSlots] every consumer has copied it
   uint64_t *stage_ok = seg_empty + kSegSlots;   // outgoing copies have read the P tiles
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(stage_ok + 1);
+  uint64_t *epi_done = stage_ok + 1;            // every warp's epilogue staging has been read
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(epi_done + 1);
   Seg *segq = reinterpret_cast<Seg *>(smem + kOffSegQ);   // [kSegSlots]
   static_assert(sizeof(Seg) <= 64, "segment descriptor slot");
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
@@ -886,6 +887,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       mbar_init(&seg_empty[s], 5);  // the MMA thread and lane 0 of each softmax warp
     }
     mbar_init(stage_ok, 4);         // lane 0 of each softmax warp, once per segment
+    mbar_init(epi_done, 4);         // likewise
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -936,6 +938,16 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     while (ok && walk.next(sg)) {
       sg.len = __ldg(args.seq_lens + sg.b);
       if (!(ok = publish(nseg, false))) break;
+      // The segment's query rows (contiguous, 1152 B each) are read by the
+      // softmax warps when this CTA reaches the segment, about a ring's
+      // worth of tiles from now; a demand load at that point waits behind
+      // every SM's KV stream, so they are pulled into L2 here.
+      if (lane == 0) {
+        const uint8_t *qrows = args.q + static_cast<int64_t>(sg.row0) * kDqk * 2;
+        const uint32_t bytes = static_cast<uint32_t>(sg.hrows) * kDqk * 2;
+        for (uint32_t o = 0; o < bytes; o += 16384)
+          prefetch_l2(qrows + o, min(16384u, bytes - o));
+      }
       const int32_t *bt = args.block_table + static_cast<int64_t>(sg.b) * args.max_blocks;
       int page_base = -(1 << 30), my_blk = -1;
       auto blk_of = [&](int tile) -> int {  // warp-collective
@@ -969,7 +981,10 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
         ++kc;
         return true;
       };
-      const int pre = min(sg.ntiles, kStages);
+      // The first KV tile of the segment, then its query rope half: the
+      // previous segment's last QK (which frees the rope buffer) completes
+      // about when the stage of this first tile frees up.
+      const int pre = min(sg.ntiles, 1);
       for (int t = 0; ok && t < pre; ++t) ok = load_tile(sg.tile0 + t);
       if (!ok) break;
       if (nseg > 0 && !(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
@@ -997,7 +1012,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       bool ok = true;
       // `chunk_c` is a std::integral_constant so the descriptor offsets are
       // compile-time constants.
-      auto issue_qk_chunk_c = [&](int kcx, int ucx, auto chunk_c) {
+      auto issue_qk_chunk_c = [&](int kcx, int ucx, bool last, auto chunk_c) {
         constexpr int chunk = decltype(chunk_c)::value;
         const uint32_t stage = smem_u32(sm_kv + (kcx % kStages) * kStageBytes);
         const uint32_t d = tmem + kColS + kTile * (ucx & 1);
@@ -1015,14 +1030,19 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
             mma_f16_ss(d, adesc, bdesc, idesc_qk, 1u);
           }
         }
-        if (chunk == kQkChunks - 1) mma_commit(&s_full[ucx & 1]);
+        if (chunk == kQkChunks - 1) {
+          mma_commit(&s_full[ucx & 1]);
+          // the segment's last QK: its query rope half in shared memory is
+          // no longer read, the next segment's may be loaded
+          if (last) mma_commit(q_free);
+        }
       };
-      auto issue_qk_chunk = [&](int kcx, int ucx, int chunk) {
+      auto issue_qk_chunk = [&](int kcx, int ucx, bool last, int chunk) {
         static_assert(kQkChunks == 3, "dispatch below covers three chunks");
         switch (chunk) {
-          case 0: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 0>{}); break;
-          case 1: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 1>{}); break;
-          default: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 2>{}); break;
+          case 0: issue_qk_chunk_c(kcx, ucx, last, std::integral_constant<int, 0>{}); break;
+          case 1: issue_qk_chunk_c(kcx, ucx, last, std::integral_constant<int, 1>{}); break;
+          default: issue_qk_chunk_c(kcx, ucx, last, std::integral_constant<int, 2>{}); break;
         }
       };
       // QK of global tile u may start once its KV tile has landed and both
@@ -1054,7 +1074,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           if (qn < sg.ntiles && qn < t + 3 &&
               (qchunks > 0 || qk_ready(kc + (qn - t), uc + (qn - t)))) {
             if (qchunks == 0) tc_fence_after();
-            issue_qk_chunk(kc + (qn - t), uc + (qn - t), qchunks);
+            issue_qk_chunk(kc + (qn - t), uc + (qn - t), qn + 1 == sg.ntiles, qchunks);
             if (++qchunks == kQkChunks) { qchunks = 0; ++qn; }
             progressed = true;
           }
@@ -1073,7 +1093,6 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
             }
             mma_commit(&kv_empty[kc % kStages]);
             mma_commit(&pv_done[uc & 1]);
-            if (t + 1 == sg.ntiles) mma_commit(q_free);
             ++t; ++kc; ++uc;
             progressed = true;
           }
@@ -1128,8 +1147,11 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       tc_fence_before();
       mbar_arrive(q_tmem);
     };
-    // Forwarded rows: partial scores of tile k (global count) -> the peer.
-    auto send_s = [&](int k) -> bool {
+    // Forwarded rows: partial scores of tile k (global count) -> s_send.
+    // The staging buffer is free as soon as this warp's copy of tile k-1 has
+    // been read out of it, which is usually long before the peer has
+    // consumed that message, so staging runs ahead of the peer.
+    auto stage_s = [&](int k) -> bool {
       if (!warp_ok(mbar_wait(&s_full[k & 1], (k >> 1) & 1, abort_flag))) return false;
       tc_fence_after();
       uint32_t sv[kTile];
@@ -1137,16 +1159,24 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       tmem_ld_x32(lane_base + kColS + kTile * (k & 1) + 32, sv + 32);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[k & 1]);   // this warp's score rows are read
-      // the peer has consumed message k-1, so s_send and its s_recv are free
-      if (k > 0 && !warp_ok(mbar_wait(xs_free, (k - 1) & 1, abort_flag))) return false;
+      if (lane == 0) {
+        mbar_arrive(&s_free[k & 1]);   // this warp's score rows are read
+        bulk_wait_read_all();          // its copy of tile k-1 has left s_send
+      }
+      __syncwarp();
       uint4 *dst = reinterpret_cast<uint4 *>(s_send + lr * 256);
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         dst[j ^ (lr & 15)] = make_uint4(sv[4 * j], sv[4 * j + 1], sv[4 * j + 2], sv[4 * j + 3]);
       fence_proxy_async_smem();
       __syncwarp();
-      // this warp's 32 rows (8 KB, contiguous) -> the same place in the peer
+      return true;
+    };
+    // Staged scores of tile k -> the peer, once it has consumed message k-1
+    // (its s_recv is free): this warp's 32 rows, 8 KB contiguous, to the
+    // same place in the peer.
+    auto post_s = [&](int k) -> bool {
+      if (k > 0 && !warp_ok(mbar_wait(xs_free, (k - 1) & 1, abort_flag))) return false;
       if (lane == 0)
         bulk_copy_to_peer(peer_s_recv + wl * (kSMsg / 2), s_send + wl * (kSMsg / 2), kSMsg / 2,
                           peer_xs_full);
@@ -1171,9 +1201,9 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     if (have) load_q_tmem(sg);
     Seg nxt;
     bool have_next = false;
-    float lq_in = 1.f;   // forwarded rows: the owner's running sum, last message
+    float l_in = 1.f;   // forwarded rows: the owner's running sum, last message
     while (ok && have) {
-      float m = -INFINITY, l = 0.f, lq = 0.f;
+      float m = -INFINITY, l = 0.f;
       const int len = sg.len;
       for (int t = 0; t < sg.ntiles; ++t, ++uc) {
         const int sb = uc & 1;
@@ -1210,17 +1240,15 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                       __uint_as_float(sr[4 * k + 3]), __uint_as_float(v.z), __uint_as_float(v.w));
           }
           // interior tiles (every position inside [lo, hi)) skip the mask
-          if (full_tile) {
-#pragma unroll
-            for (int k = 0; k < kTile; ++k) mx[k & 3] = fmaxf(mx[k & 3], x[k]);
-          } else {
+          if (!full_tile) {
 #pragma unroll
             for (int k = 0; k < kTile; ++k) {
               const int pos = pos0 + k;
               x[k] = (pos >= sg.lo && pos < sg.hi) ? x[k] : -INFINITY;
-              mx[k & 3] = fmaxf(mx[k & 3], x[k]);
             }
           }
+#pragma unroll
+          for (int k = 0; k < kTile; k += 2) mx[(k >> 1) & 3] = fmax3(mx[(k >> 1) & 3], x[k], x[k + 1]);
           __syncwarp();
           if (lane == 0) mbar_arrive_remote(peer_xs_free);   // this warp's rows of s_recv are consumed
           const float tmax =
@@ -1245,21 +1273,22 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                 tmem_st_x32(lane_base + kColO + c, o);
               }
               l *= alpha;
-              lq *= alpha;
               if (need) m = m_new;
             }
           } else {
             m = tmax;
           }
           // p = 2^(s * scale - m): paired FMAs, then the hardware ex2; the
-          // row sums accumulate in pairs (four chains)
+          // row sum accumulates in pairs (four chains).  It serves both the
+          // LSE and the normalisation of O (bf16 rounding of P moves the
+          // weights by ~2^-9 relative, far inside the output tolerance).
           const float nm = -m, sc = args.scale_log2;
 #pragma unroll
           for (int k = 0; k < kTile; k += 2)
             fma_f32x2(x[k], x[k + 1], x[k], x[k + 1], sc, sc, nm, nm);
 #pragma unroll
           for (int k = 0; k < kTile; ++k) x[k] = ex2(x[k]);
-          float ps[4] = {0.f, 0.f, 0.f, 0.f}, qs[4] = {0.f, 0.f, 0.f, 0.f};
+          float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int k = 0; k < kTile; k += 4) {
             add_f32x2(ps[0], ps[1], ps[0], ps[1], x[k], x[k + 1]);
@@ -1269,14 +1298,6 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           uint32_t pk[kTile / 2];
 #pragma unroll
           for (int k = 0; k < kTile / 2; ++k) pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
-#pragma unroll
-          for (int k = 0; k < kTile / 2; k += 2) {
-            add_f32x2(qs[0], qs[1], qs[0], qs[1], __uint_as_float(pk[k] << 16),
-                      __uint_as_float(pk[k] & 0xFFFF0000u));
-            add_f32x2(qs[2], qs[3], qs[2], qs[3], __uint_as_float(pk[k + 1] << 16),
-                      __uint_as_float(pk[k + 1] & 0xFFFF0000u));
-          }
-          lq += (qs[0] + qs[1]) + (qs[2] + qs[3]);
           // P tile `sb` and the factor slot are free once P.V of tile uc-2
           // is done here (and the copy out of them has landed) and in the
           // peer (which takes our rows into its own P tile)
@@ -1291,10 +1312,10 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
 #pragma unroll
           for (int j = 0; j < 8; ++j)
             prow[j ^ (r & 7)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-          // factors of this warp's rows: alpha[32] then lq[32]
+          // factors of this warp's rows: alpha[32] then the running sum l[32]
           float *al = reinterpret_cast<float *>(al_send + sb * kAlMsg + wl * (kAlMsg / 2));
           al[lane] = alpha;
-          al[32 + lane] = lq;
+          al[32 + lane] = l;
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
@@ -1315,27 +1336,32 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
             if (mbar_wait(&pv_done[sb], (up >> 1) & 1, abort_flag))
               mbar_arrive_remote(peer_smem(&pb_free[sb], peer));
           }
-          // The scores of the next tile of this segment go out as soon as
-          // QK has produced them, before or after the probabilities of this
-          // tile come back, whichever is possible first.  (Not across a
-          // segment end: the next segment's QK needs the query these
-          // threads stage after the segment's last tile.)
-          if (t == 0) ok = send_s(uc);
+          // The scores of the next tile of this segment are staged as soon
+          // as QK has produced them and go out as soon as the peer has
+          // consumed the previous message, before or after the
+          // probabilities of this tile come back, whichever is possible
+          // first.  (Not across a segment end: the next segment's QK needs
+          // the query these threads stage after the segment's last tile.)
+          if (t == 0) ok = stage_s(uc) && post_s(uc);
           if (!ok) break;
           if (leader) mbar_arrive_expect_tx(&xp_full[sb], kPMsg);
-          bool pending = t + 1 < sg.ntiles, got_p = false;
+          bool pending = t + 1 < sg.ntiles, staged = false, got_p = false;
           long long t_spin = 0;
           while (pending || !got_p) {
             bool progressed = false;
-            if (pending) {
-              const bool ready = mbar_test(&s_full[(uc + 1) & 1], ((uc + 1) >> 1) & 1) &&
-                                 mbar_test(xs_free, uc & 1);
-              if (__shfl_sync(0xffffffffu, ready, 0)) {
-                ok = send_s(uc + 1);
+            if (pending && !staged) {
+              if (__shfl_sync(0xffffffffu,
+                              mbar_test(&s_full[(uc + 1) & 1], ((uc + 1) >> 1) & 1), 0)) {
+                ok = stage_s(uc + 1);
                 if (!ok) break;
-                pending = false;
+                staged = true;
                 progressed = true;
               }
+            } else if (pending && __shfl_sync(0xffffffffu, mbar_test(xs_free, uc & 1), 0)) {
+              ok = post_s(uc + 1);
+              if (!ok) break;
+              pending = false;
+              progressed = true;
             }
             if (!got_p && __shfl_sync(0xffffffffu, mbar_test(&xp_full[sb], (uc >> 1) & 1), 0)) {
               got_p = true;
@@ -1352,7 +1378,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           const float *al =
               reinterpret_cast<const float *>(al_recv + sb * kAlMsg + wl * (kAlMsg / 2));
           const float alpha = al[lane];
-          lq_in = al[32 + lane];
+          l_in = al[32 + lane];
           if (t > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
             const int up = uc - 1;
             ok = warp_ok(mbar_wait(&pv_done[up & 1], (up >> 1) & 1, abort_flag));
@@ -1402,8 +1428,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       }
       if (!ok) break;
       tc_fence_after();
-      // The epilogue stages through P tile 0: every bulk copy out of the P
-      // tiles (this CTA's rows of P to the peer) must have been read first.
+      // The epilogue stages through the P tiles: every bulk copy out of
+      // them (this CTA's rows of P to the peer) must have been read first.
       if (lane == 0) {
         bulk_wait_read_all();
         mbar_arrive(stage_ok);
@@ -1413,66 +1439,128 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       const Seg cur = sg;
       sg = nxt;
       have = have_next;
-      // ---- epilogue: O / lq for this CTA's 256 latent columns, all rows.
-      // Each warp stages 32 rows x 32 columns at a time in its 4 KB slice of
-      // the P tiles (idle now: P.V of this segment is done and the peer
-      // sends the next segment's P only after our signal for it), so every
-      // store instruction writes whole row segments instead of one 16-byte
-      // piece of 32 different rows.
-      const float inv = args.out_scale / (own ? lq : lq_in);
+      // ---- epilogue: O / l for this CTA's 256 latent columns, all rows.
+      const float inv = args.out_scale / (own ? l : l_in);
       const bool row_ok = r < cur.hrows;
       const bool bf16_out = cur.whole && args.out_dtype == MLA_BF16;
-      uint4 *stage = reinterpret_cast<uint4 *>(sm_p + (warp - 2) * 4096);
+      if (!cur.whole || cur.hrows == 128) {
+        // Every row of this warp's 32-row box belongs to the job (a partial
+        // slot always has 128 rows): tensor-map stores of 128-byte rows
+        // (32 fp32 or 64 bf16 columns) from two 4 KB staging buffers per
+        // warp in the idle P tiles, 128B-swizzled; lane 0 issues them and
+        // the TMA engine drains them while the warp moves on.
+        const CUtensorMap *tm = cur.whole ? &tm_out : &tm_ws;
+        const int y = (cur.whole ? cur.out_row0 : cur.slot * 128) + quarter * 32;
+        uint8_t *stg = sm_p + (warp - 2) * 8192;
 #pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
-        uint32_t o[32];
-        tmem_ld_x32(lane_base + kColO + c, o);
-        float v[32];
+        for (int c = 0; c < 256; c += 64) {
+          // 64 columns per step; the TMEM read goes out before the wait for
+          // the staging buffers, so the two latencies overlap
+          uint32_t o[64];
+          tmem_ld_x64(lane_base + kColO + c, o);
+          auto f = [&](int k) { return __uint_as_float(o[k]) * inv; };
+          if (bf16_out) {
+            // one 4 KB box per step, the two buffers alternating
+            uint8_t *buf = stg + ((c >> 6) & 1) * 4096;
+            if (c >= 128) {
+              if (lane == 0) bulk_wait_read_1();   // the store two steps back has read `buf`
+              __syncwarp();
+            }
+            uint4 *row = reinterpret_cast<uint4 *>(buf + lane * 128);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
-        if (bf16_out) {
-          // row = 64 bytes = 4 chunks of 8 bf16
+            for (int k = 0; k < 8; ++k)
+              row[k ^ (lane & 7)] =
+                  make_uint4(pack_bf16(f(8 * k), f(8 * k + 1)), pack_bf16(f(8 * k + 2), f(8 * k + 3)),
+                             pack_bf16(f(8 * k + 4), f(8 * k + 5)), pack_bf16(f(8 * k + 6), f(8 * k + 7)));
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) tma_store_2d(tm, buf, 256 * half + c, y);
+          } else {
+            // two 4 KB boxes of 32 fp32 columns per step
+            if (c > 0) {
+              if (lane == 0) bulk_wait_read_all();   // the previous step's stores have read both
+              __syncwarp();
+            }
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            stage[lane * 4 + (k ^ (lane & 3))] =
-                make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]), pack_bf16(v[8 * k + 2], v[8 * k + 3]),
-                           pack_bf16(v[8 * k + 4], v[8 * k + 5]), pack_bf16(v[8 * k + 6], v[8 * k + 7]));
-        } else {
-          // row = 128 bytes = 8 chunks of 4 fp32
+            for (int hh = 0; hh < 2; ++hh) {
+              uint4 *row = reinterpret_cast<uint4 *>(stg + hh * 4096 + lane * 128);
 #pragma unroll
-          for (int k = 0; k < 8; ++k)
-            stage[lane * 8 + (k ^ (lane & 7))] =
-                make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
-                           __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
-        }
-        __syncwarp();
-        const int col = 256 * half + c;
-        if (bf16_out) {
-#pragma unroll
-          for (int it = 0; it < 4; ++it) {
-            const int row = it * 8 + (lane >> 2), ch = lane & 3;   // 8 rows per instruction
-            const int R = quarter * 32 + row;
-            if (R < cur.hrows)
-              reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.out) +
-                                        static_cast<int64_t>(cur.out_row0 + R) * kLatent + col)[ch] =
-                  stage[row * 4 + (ch ^ (row & 3))];
-          }
-        } else {
-#pragma unroll
-          for (int it = 0; it < 8; ++it) {
-            const int row = it * 4 + (lane >> 3), ch = lane & 7;   // 4 rows per instruction
-            const int R = quarter * 32 + row;
-            if (R < cur.hrows) {
-              float *base = cur.whole
-                                ? static_cast<float *>(args.out) +
-                                      static_cast<int64_t>(cur.out_row0 + R) * kLatent + col
-                                : args.ws_o + (static_cast<int64_t>(cur.slot) * 128 + R) * kLatent + col;
-              reinterpret_cast<uint4 *>(base)[ch] = stage[row * 8 + (ch ^ (row & 7))];
+              for (int k = 0; k < 8; ++k)
+                row[k ^ (lane & 7)] =
+                    make_uint4(__float_as_uint(f(32 * hh + 4 * k)), __float_as_uint(f(32 * hh + 4 * k + 1)),
+                               __float_as_uint(f(32 * hh + 4 * k + 2)),
+                               __float_as_uint(f(32 * hh + 4 * k + 3)));
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(tm, stg, 256 * half + c, y);
+              tma_store_2d(tm, stg + 4096, 256 * half + c + 32, y);
             }
           }
         }
+        if (lane == 0) bulk_wait_read_all();
         __syncwarp();
+      } else {
+        // A head group with fewer than 128 rows, written whole: the rows
+        // past it belong to the next query row's heads, so only valid rows
+        // are stored, staged per 32 columns for whole-row-segment stores.
+        uint4 *stage = reinterpret_cast<uint4 *>(sm_p + (warp - 2) * 4096);
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+          uint32_t o[32];
+          tmem_ld_x32(lane_base + kColO + c, o);
+          float v[32];
+#pragma unroll
+          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
+          if (bf16_out) {
+            // row = 64 bytes = 4 chunks of 8 bf16
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+              stage[lane * 4 + (k ^ (lane & 3))] =
+                  make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]), pack_bf16(v[8 * k + 2], v[8 * k + 3]),
+                             pack_bf16(v[8 * k + 4], v[8 * k + 5]), pack_bf16(v[8 * k + 6], v[8 * k + 7]));
+          } else {
+            // row = 128 bytes = 8 chunks of 4 fp32
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              stage[lane * 8 + (k ^ (lane & 7))] =
+                  make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
+                             __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
+          }
+          __syncwarp();
+          const int col = 256 * half + c;
+          if (bf16_out) {
+#pragma unroll
+            for (int it = 0; it < 4; ++it) {
+              const int row = it * 8 + (lane >> 2), ch = lane & 3;   // 8 rows per instruction
+              const int R = quarter * 32 + row;
+              if (R < cur.hrows)
+                reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.out) +
+                                          static_cast<int64_t>(cur.out_row0 + R) * kLatent + col)[ch] =
+                    stage[row * 4 + (ch ^ (row & 3))];
+            }
+          } else {
+#pragma unroll
+            for (int it = 0; it < 8; ++it) {
+              const int row = it * 4 + (lane >> 3), ch = lane & 7;   // 4 rows per instruction
+              const int R = quarter * 32 + row;
+              if (R < cur.hrows) {
+                float *base = static_cast<float *>(args.out) +
+                              static_cast<int64_t>(cur.out_row0 + R) * kLatent + col;
+                reinterpret_cast<uint4 *>(base)[ch] = stage[row * 8 + (ch ^ (row & 7))];
+              }
+            }
+          }
+          __syncwarp();
+        }
       }
+      // The P tiles are written again in the next segment (own rows, and
+      // the peer's rows after our signal), also by other warps of this CTA:
+      // every warp's staging has been read out first.
+      if (lane == 0) mbar_arrive(epi_done);
+      ok = warp_ok(mbar_wait(epi_done, (ns - 2) & 1, abort_flag));
+      if (!ok) break;
       const int64_t orow = static_cast<int64_t>(cur.out_row0 + r);
       if (row_ok && own) {
         const float lse = (m + log2f(l)) * 0.69314718055994531f;
@@ -1668,7 +1756,7 @@ int launch_decode(const void *q, const void *kv_cache, int B, int q_len, int H,
 }
 
 int launch_decode_pair(const void *q, const void *kv_cache, int B, int q_len, int H,
-                       int num_blocks, DecodeArgs a, mla_stream_t stream) {
+                       int num_blocks, int64_t ws_slots, DecodeArgs a, mla_stream_t stream) {
   // KV latent boxes {64 columns, 64 tokens} (128B swizzle); KV and query
   // rope halves {32 columns, 64 tokens / 128 heads} (64B swizzle)
   CUtensorMap tm_kv, tm_kr, tm_qr;
@@ -1686,11 +1774,28 @@ int launch_decode_pair(const void *q, const void *kv_cache, int B, int q_len, in
       !make_tmap(&tm_qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, q_dims, strides, box_qr,
                  CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
+  // Epilogue stores: 32-row boxes of 128-byte rows (32 fp32 or 64 bf16),
+  // 128B swizzle, into the output [rows, 512] and the partials [slots*128, 512].
+  CUtensorMap tm_out, tm_ws;
+  const bool out_bf16 = a.out_dtype == MLA_BF16;
+  const uint64_t out_dims[2] = {kLatent, static_cast<uint64_t>(B) * q_len * H};
+  const uint64_t out_strides[1] = {static_cast<uint64_t>(kLatent) * (out_bf16 ? 2 : 4)};
+  const uint32_t box_out[2] = {out_bf16 ? 64u : 32u, 32};
+  const uint64_t ws_dims[2] = {kLatent, static_cast<uint64_t>(ws_slots) * 128};
+  const uint64_t ws_strides[1] = {static_cast<uint64_t>(kLatent) * 4};
+  const uint32_t box_ws[2] = {32, 32};
+  if (!make_tmap(&tm_out,
+                 out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+                 a.out, out_dims, out_strides, box_out, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap(&tm_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.ws_o, ws_dims, ws_strides, box_ws,
+                 CU_TENSOR_MAP_SWIZZLE_128B))
+    return MLA_ERR_CUDA;
   if (cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            pair::kSmem) != cudaSuccess)
     return MLA_ERR_CUDA;
   PairLaunch pl(a.groups, stream);
-  if (cudaLaunchKernelEx(&pl.cfg, decode_pair_kernel, tm_kv, tm_kr, tm_qr, a) != cudaSuccess)
+  if (cudaLaunchKernelEx(&pl.cfg, decode_pair_kernel, tm_kv, tm_kr, tm_qr, tm_out, tm_ws, a) !=
+      cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }
@@ -1764,7 +1869,8 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   a.ws_lse = ws_lse;
   a.err = err;
   const int st = fp8 ? launch_decode<true>(q, kv_cache, B, q_len, H, num_blocks, a, stream)
-                     : launch_decode_pair(q, kv_cache, B, q_len, H, num_blocks, a, stream);
+                     : launch_decode_pair(q, kv_cache, B, q_len, H, num_blocks, w.slots, a,
+                                          stream);
   if (st != MLA_OK) return st;
 
   const int64_t rows = static_cast<int64_t>(J) * 128;

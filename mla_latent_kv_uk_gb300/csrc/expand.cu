@@ -39,8 +39,7 @@ struct ExpandArgs {
 };
 
 __device__ __forceinline__ uint32_t pack2(float a, float b) {
-  return static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(a))) |
-         (static_cast<uint32_t>(__bfloat16_as_ushort(__float2bfloat16_rn(b))) << 16);
+  return bf16x2_rn(a, b);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)

@@ -8,6 +8,8 @@
 #include <cuda_bf16.h>
 #include <math.h>
 
+#include "sm100.cuh"
+
 namespace mla {
 
 __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float *v) {
@@ -30,11 +32,7 @@ __device__ __forceinline__ void load8(const float *p, float *v) {
 __device__ __forceinline__ void store8(__nv_bfloat16 *p, const float *v) {
   uint32_t w[4];
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    uint32_t lo = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * k]));
-    uint32_t hi = __bfloat16_as_ushort(__float2bfloat16_rn(v[2 * k + 1]));
-    w[k] = lo | (hi << 16);
-  }
+  for (int k = 0; k < 4; ++k) w[k] = sm100::bf16x2_rn(v[2 * k], v[2 * k + 1]);
   *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
 }
 
