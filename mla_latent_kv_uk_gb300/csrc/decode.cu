@@ -1133,17 +1133,16 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                              args.q + static_cast<int64_t>(seg.row0 + r) * kDqk * 2) +
                          32 * half;
       const bool valid = r < seg.hrows;
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        uint32_t w[64];
+      // all 32 loads in flight at once: under the KV stream every round
+      // trip to memory costs thousands of cycles
+      uint32_t w[128];
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          uint4 v = valid ? __ldg(src + c * 16 + k) : make_uint4(0, 0, 0, 0);
-          w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
-        }
-        tmem_st_x32(lane_base + kColQ + 64 * c, w);
-        tmem_st_x32(lane_base + kColQ + 64 * c + 32, w + 32);
+      for (int k = 0; k < 32; ++k) {
+        uint4 v = valid ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
+        w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
       }
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_st_x32(lane_base + kColQ + 32 * c, w + 32 * c);
       tc_fence_before();
       mbar_arrive(q_tmem);
     };
