@@ -72,22 +72,31 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
 }
 
 // ------------------------------------------------------------------ absorb
-// smem: A [2 K-chunks][4 l-blocks] of {64 l x 64 p} boxes (64 KB),
-//       B [2 K-chunks] of {64 p x NT t} (NT * 128 B each), staging 32 KB.
+// smem: A [2 K-chunks][4 l-blocks] of {64 l x 64 p} boxes (64 KB; once the
+//       MMAs are done it stages the output), B [2 K-chunks] of {64 p x NT t}
+//       (NT * 128 B each), the q_pe tile {64 x NT t} (latent half 1 only;
+//       room for NT rounded up to 32 rows, as its chunks are stored whole).
+// The output leaves through tensor-map stores: per 32-token chunk one box
+// of this CTA's 256 latent columns and, for half 1, one of the 64 rope
+// columns (straight from the q_pe tile when the output is bf16).
 __global__ void __launch_bounds__(kThreads, 1)
 absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
-              const __grid_constant__ CUtensorMap tm_q, GemmArgs args) {
+              const __grid_constant__ CUtensorMap tm_q,
+              const __grid_constant__ CUtensorMap tm_qpe,
+              const __grid_constant__ CUtensorMap tm_out,
+              const __grid_constant__ CUtensorMap tm_out_pe, GemmArgs args) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NT = args.NT;
   uint8_t *sm_a = smem;                          // 64 KB
   uint8_t *sm_b = smem + 8 * kBoxBytes64;        // 2 * NT * 128
-  uint8_t *sm_o = sm_b + 2 * NT * 128;           // 32 tokens x 256 x 4 B
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_o + kStageTokens * 256 * 4);
+  uint8_t *sm_pe = sm_b + 2 * NT * 128;          // round_up(NT, 32) * 128
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_pe + ((NT + 31) / 32) * 32 * 128);
   uint64_t *full = bars, *done = bars + 1, *drain = bars + 2;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 3);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *go = abort_flag + 1;             // the epilogue's common decision
 
   const int warp = warp_id(), lane = lane_id();
   const int mh = blockIdx.x;          // latent half: l in [256 mh, 256 mh + 256)
@@ -119,13 +128,14 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_q);
-    mbar_arrive_expect_tx(full, 8 * kBoxBytes64 + 2 * NT * 128);
+    mbar_arrive_expect_tx(full, 8 * kBoxBytes64 + 2 * NT * 128 + (mh == 1 ? NT * 128 : 0));
     for (int kc = 0; kc < 2; ++kc) {
       for (int lb = 0; lb < 4; ++lb)   // W_UK_T as [H*128 rows (p), 512 cols (l)]
         tma_load_2d(sm_a + (kc * 4 + lb) * kBoxBytes64, &tm_w, full,
                     256 * mh + 64 * lb, h * 128 + 64 * kc);
       tma_load_3d(sm_b + kc * NT * 128, &tm_q, full, 64 * kc, h, t0);
     }
+    if (mh == 1) tma_load_3d(sm_pe, &tm_qpe, full, 0, h, t0);
     if (!mbar_wait(full, 0, abort_flag)) {
       volatile int no_abort = 0;
       mbar_wait(full, 0, &no_abort);
@@ -160,47 +170,48 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
     const int quarter = warp & 3;
     const int lrow = quarter * 32 + lane;       // latent row within an M chunk
     const int dt = args.out_dtype, es = esize(dt);
-    const bool ok = mbar_wait(done, 0, abort_flag);
+    mbar_wait(done, 0, abort_flag);
+    // one decision for all four warps (a timed-out wait has set the flag
+    // before this barrier), so none is left alone at the barriers below
+    epi_bar();
+    if (tid == 0) *go = *abort_flag ? 0 : 1;
+    epi_bar();
     tc_fence_after();
-    if (ok) {
-      const int row_bytes = 256 * es;           // this CTA's half of a token row
+    if (*go) {
+      // the MMAs have read A and B: A's 64 KB hold the staging
+      uint8_t *stg = sm_a;                      // [32 t][256 l] in the output dtype
+      uint8_t *stg_pe = sm_a + kStageTokens * 256 * 4;   // [32 t][64]
       for (int c0 = 0; c0 < ntok; c0 += kStageTokens) {
+        if (c0 > 0) {   // the previous chunk's stores have read the staging
+          if (tid == 0) bulk_wait_read_all();
+          epi_bar();
+        }
         for (int mc = 0; mc < 2; ++mc) {
           uint32_t r[32];
           tmem_ld_x32(tmem_addr(tmem, warp, mc * cols + c0), r);
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            put(sm_o + c * row_bytes + (mc * 128 + lrow) * es, dt, __uint_as_float(r[c]),
-                args.q_scale);
+            put(stg + (c * 256 + mc * 128 + lrow) * es, dt, __uint_as_float(r[c]), args.q_scale);
         }
-        epi_bar();
-        const int nt = min(kStageTokens, ntok - c0);
-        const int chunks = row_bytes / 16;
-        uint8_t *out = static_cast<uint8_t *>(args.out);
-        for (int i = tid; i < nt * chunks; i += 128) {
-          const int t = t0 + c0 + i / chunks, c = i % chunks;
-          const int64_t base = ((static_cast<int64_t>(t) * args.H + h) * kDqk + 256 * mh) * es;
-          reinterpret_cast<uint4 *>(out + base)[c] =
-              reinterpret_cast<const uint4 *>(sm_o + (i / chunks) * row_bytes)[c];
-        }
-        epi_bar();
-      }
-      if (mh == 1) {
-        // q_pe columns 512..575 of every token in the tile, 8 per thread
-        uint8_t *out = static_cast<uint8_t *>(args.out);
-        for (int i = tid; i < ntok * 8; i += 128) {
-          const int t = t0 + i / 8, c = (i % 8) * 8;
-          const uint4 raw = __ldg(reinterpret_cast<const uint4 *>(
-              args.q_pe + (static_cast<int64_t>(t) * args.H + h) * kRope + c));
-          const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-          const int64_t base = ((static_cast<int64_t>(t) * args.H + h) * kDqk + kLatent + c) * es;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const float v = __uint_as_float((k & 1) ? (w[k >> 1] & 0xFFFF0000u) : (w[k >> 1] << 16));
-            put(out + base + k * es, dt, v, args.q_scale);
+        if (mh == 1 && dt != MLA_BF16) {
+          // rope columns in the output dtype (bf16 leaves from its own tile)
+          for (int i = tid; i < kStageTokens * 64; i += 128) {
+            const int t = i >> 6, c = i & 63;
+            const uint32_t raw = reinterpret_cast<const uint16_t *>(sm_pe + (c0 + t) * 128)[c];
+            put(stg_pe + (t * 64 + c) * es, dt, __uint_as_float(raw << 16), args.q_scale);
           }
         }
+        fence_proxy_async_smem();
+        epi_bar();
+        if (tid == 0) {
+          tma_store_3d(&tm_out, stg, 256 * mh, h, t0 + c0);
+          if (mh == 1)
+            tma_store_3d(&tm_out_pe, dt == MLA_BF16 ? sm_pe + c0 * 128 : stg_pe, kLatent, h,
+                         t0 + c0);
+        }
       }
+      // the stores have completed before this CTA's shared memory is released
+      if (tid == 0) bulk_wait_all();
     }
     tc_fence_before();
   }
@@ -228,6 +239,7 @@ vup_kernel(const __grid_constant__ CUtensorMap tm_w,
   uint64_t *full = bars, *empty = bars + 8, *done = bars + 16, *drain = bars + 17;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 18);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
+  volatile int *go = abort_flag + 1;             // the epilogue's common decision
   const int warp = warp_id(), lane = lane_id();
   const int h = blockIdx.x;
   const int t0 = blockIdx.y * NT;
@@ -297,9 +309,14 @@ vup_kernel(const __grid_constant__ CUtensorMap tm_w,
   } else if (warp >= 2) {
     const int tid = threadIdx.x - 64;
     const int v = (warp & 3) * 32 + lane;
-    const bool ok = mbar_wait(done, 0, abort_flag);
+    mbar_wait(done, 0, abort_flag);
+    // one decision for all four warps (a timed-out wait has set the flag
+    // before this barrier), so none is left alone at the barriers below
+    epi_bar();
+    if (tid == 0) *go = *abort_flag ? 0 : 1;
+    epi_bar();
     tc_fence_after();
-    if (ok) {
+    if (*go) {
       for (int c0 = 0; c0 < ntok; c0 += kStageTokens) {
         uint32_t r[32];
         tmem_ld_x32(tmem_addr(tmem, warp, c0), r);
@@ -372,14 +389,42 @@ extern "C" int mla_absorb_q(const void *q_nope, const void *q_pe,
                    strides, box, CU_TENSOR_MAP_SWIZZLE_128B))
       return MLA_ERR_CUDA;
   }
+  // q_pe [T, H, 64] rows in, and the output [T, H, 576] in boxes of 32
+  // tokens x (256 latent | 64 rope) columns out, no swizzle
+  CUtensorMap tpe, to_lat, to_pe;
+  {
+    const uint64_t dims[3] = {static_cast<uint64_t>(kRope), static_cast<uint64_t>(H),
+                              static_cast<uint64_t>(T)};
+    const uint64_t strides[2] = {kRope * 2, static_cast<uint64_t>(H) * kRope * 2};
+    const uint32_t box[3] = {static_cast<uint32_t>(kRope), 1, static_cast<uint32_t>(NT)};
+    if (!make_tmap(&tpe, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, q_pe, dims, strides, box,
+                   CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MLA_ERR_CUDA;
+  }
+  {
+    const uint64_t es = out_dtype == MLA_F32 ? 4 : out_dtype == MLA_BF16 ? 2 : 1;
+    const CUtensorMapDataType tdt = out_dtype == MLA_F32    ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                    : out_dtype == MLA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                            : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const uint64_t dims[3] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(H),
+                              static_cast<uint64_t>(T)};
+    const uint64_t strides[2] = {kDqk * es, static_cast<uint64_t>(H) * kDqk * es};
+    const uint32_t box_lat[3] = {256, 1, static_cast<uint32_t>(kStageTokens)};
+    const uint32_t box_pe[3] = {static_cast<uint32_t>(kRope), 1,
+                                static_cast<uint32_t>(kStageTokens)};
+    if (!make_tmap(&to_lat, tdt, 3, q_out, dims, strides, box_lat, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !make_tmap(&to_pe, tdt, 3, q_out, dims, strides, box_pe, CU_TENSOR_MAP_SWIZZLE_NONE))
+      return MLA_ERR_CUDA;
+  }
   GemmArgs a{T, H, NT, out_dtype, q_scale,
              static_cast<const __nv_bfloat16 *>(q_pe), q_out, err};
-  const size_t smem = 1024 + 8 * kBoxBytes64 + 2 * NT * 128 + kStageTokens * 256 * 4 + 64;
+  const size_t smem = 1024 + 8 * kBoxBytes64 + 2 * NT * 128 + ((NT + 31) / 32) * 32 * 128 + 64;
   if (cudaFuncSetAttribute(absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MLA_ERR_CUDA;
   dim3 grid(2, H, (T + NT - 1) / NT);
-  if (launch_pdl(absorb_kernel, grid, dim3(kThreads), smem, stream, ta, tb, a) != cudaSuccess)
+  if (launch_pdl(absorb_kernel, grid, dim3(kThreads), smem, stream, ta, tb, tpe, to_lat, to_pe,
+                 a) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }

@@ -122,6 +122,15 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *map, const void 
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap *map, const void *src,
+                                             int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];"
+      ::"l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
 // Bulk prefetch of `bytes` (multiple of 16, 16-byte aligned) into L2.
 __device__ __forceinline__ void prefetch_l2(const void *src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(
