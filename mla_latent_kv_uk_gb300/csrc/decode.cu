@@ -150,6 +150,9 @@ plan_kernel(const int32_t *__restrict__ seq_lens,
   // the decode grid may be scheduled now; it waits for this grid to finish
   // before it reads the plan
   sm100::grid_dep_launch();
+  // launched with programmatic stream serialization: the lengths and
+  // ranges may come from the previous kernel in the stream
+  sm100::grid_dep_wait();
   const int J = B * q_len * HG;
   int32_t *tp = plan + 4;
   int32_t *sp = tp + (J + 1);
@@ -1715,10 +1718,11 @@ extern "C" int mla_decode_plan(const int32_t *seq_lens, const int32_t *kv_starts
   int *err = device_error_word();
   if (!err) return MLA_ERR_CUDA;
   const int tile = kv_dtype == MLA_E4M3 ? Geo<true>::kTile : Geo<false>::kTile;
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, kv_starts, kv_ends, B,
-                                              q_len, HG, max_blocks, causal ? 1 : 0,
-                                              tile, split_tiles, g, plan, err);
-  return launch_status();
+  if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, seq_lens, kv_starts,
+                 kv_ends, B, q_len, HG, max_blocks, causal ? 1 : 0, tile, split_tiles, g, plan,
+                 err) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  return MLA_OK;
 }
 
 namespace {
@@ -1842,10 +1846,10 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   float *ws_lse = reinterpret_cast<float *>(ws + w.lse_off);
 
   const int tile = fp8 ? Geo<true>::kTile : Geo<false>::kTile;
-  plan_kernel<<<1, kPlanThreads, 0, stream>>>(seq_lens, kv_starts, kv_ends, B,
-                                              q_len, HG, max_blocks, causal ? 1 : 0,
-                                              tile, split_tiles, g, plan, err);
-  if (cudaGetLastError() != cudaSuccess) return MLA_ERR_CUDA;
+  if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, seq_lens, kv_starts,
+                 kv_ends, B, q_len, HG, max_blocks, causal ? 1 : 0, tile, split_tiles, g, plan,
+                 err) != cudaSuccess)
+    return MLA_ERR_CUDA;
 
   DecodeArgs a{};
   a.plan = plan;

@@ -45,8 +45,9 @@ __device__ __forceinline__ void store8(float *p, const float *v) {
 // lse0[s * lse_stride].  D % 8 == 0, D <= 256 * NC (NC 16-byte chunk slots
 // per lane).
 //
-// Latency layout: lane s holds the LSE of part s (32 parts per pass), the
-// weights come from shuffles, and the row data of up to four parts is
+// Latency layout: up to four parts cost one round of loads (LSEs and rows
+// together); beyond that lane s holds the LSE of part s (32 parts per pass),
+// the weights come from shuffles, and the row data of up to four parts is
 // requested before any of it is used, so a row costs a few L2 round trips
 // instead of two per part.
 template <typename Tin, typename Tout, int NC = 4>
@@ -54,6 +55,60 @@ __device__ __forceinline__ void merge_row(const Tin *part0, int64_t part_stride,
                                           const float *lse0, int64_t lse_stride,
                                           int S, int D, Tout *out,
                                           float *out_lse, int lane) {
+  if (S <= 4) {
+    // Few parts (the usual split): the LSEs and every part's row go out in
+    // one round of loads; a part of weight 0 is loaded but masked by a
+    // select, so whatever it holds never reaches the output.
+    const int chunks = D / 8;
+    const float lk = lane < S ? lse0[lane * lse_stride] : -INFINITY;
+    float v[4][NC][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const Tin *p = part0 + static_cast<int64_t>(u) * part_stride;
+#pragma unroll
+      for (int i = 0; i < NC; ++i) {
+        const int c = lane + 32 * i;
+        if (u < S && c < chunks) load8(p + c * 8, v[u][i]);
+      }
+    }
+    float m = lk;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (m == -INFINITY) {
+      float zero[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+      for (int c = lane; c < chunks; c += 32) store8(out + c * 8, zero);
+      if (out_lse && lane == 0) *out_lse = -INFINITY;
+      return;
+    }
+    const float wk = lk == -INFINITY ? 0.f : expf(lk - m);
+    float z = wk;
+#pragma unroll
+    for (int o = 16; o; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+    float w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) w[u] = __shfl_sync(0xffffffffu, wk, u);
+    const float inv = 1.f / z;
+#pragma unroll
+    for (int i = 0; i < NC; ++i) {
+      const int c = lane + 32 * i;
+      if (c < chunks) {
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (u < S && w[u] != 0.f) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(w[u], v[u][i][e], acc[e]);
+          }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] *= inv;
+        store8(out + c * 8, acc);
+      }
+    }
+    if (out_lse && lane == 0) *out_lse = m + logf(z);
+    return;
+  }
   float m = -INFINITY;
   for (int s = lane; s < S; s += 32) m = fmaxf(m, lse0[s * lse_stride]);
 #pragma unroll
