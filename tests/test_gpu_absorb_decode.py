@@ -288,6 +288,22 @@ def test_decode_reruns_bit_identical(m):
         assert np.array_equal(bits(lse), lb0)
 
 
+def test_decode_many_short_jobs(m):
+    """Many jobs (B = 150 requests x 2 query tokens) of short ragged lengths,
+    empty ones included, so most spans hold several whole jobs and few are
+    split: against the oracle."""
+    g = synth.generator(470)
+    B = 150
+    seq = g.integers(0, 200, B).astype(np.int32)
+    case = synth.decode_case("many_jobs", 471, B=B, H=16, seq_lens=seq, q_len=2, poison=True)
+    out, lse = _run_decode(m, case)
+    ro, rl = _oracle_decode(case)
+    # contexts of a few tokens leave outputs near single value rows (|out| up
+    # to ~4): bf16 rounding of P and of the output, 2^-9 each, relative
+    _check(out, lse, ro, rl, out_tol=OUT_TOL + 2.0 ** -8 * float(np.abs(ro).max()))
+    assert m.mla_get_device_error() == 0
+
+
 # ------------------------------------------------------------- fp8 decode
 FP8_OUT_TOL, FP8_LSE_TOL = 5e-2, 1e-2
 
