@@ -199,6 +199,118 @@ plan_kernel(const int32_t *__restrict__ seq_lens,
   }
 }
 
+// The same plan from one warp, for up to kWarpPlanJobs jobs: every lane
+// takes ceil(J/32) <= 8 consecutive jobs, the prefixes come from warp scans
+// (no block-wide barriers on the path from the lengths to the plan).
+constexpr int kWarpPlanJobs = 256;
+
+__global__ void __launch_bounds__(32)
+plan_warp_kernel(const int32_t *__restrict__ seq_lens,
+                 const int32_t *__restrict__ kv_starts,
+                 const int32_t *__restrict__ kv_ends, int B, int q_len, int HG,
+                 int max_blocks, int causal, int tile, int forced_chunk,
+                 int groups, int32_t *plan, int *err) {
+  sm100::grid_dep_launch();
+  // launched with programmatic stream serialization: the lengths and
+  // ranges may come from the previous kernel in the stream
+  sm100::grid_dep_wait();
+  const int lane = threadIdx.x;
+  const int J = B * q_len * HG;
+  const int per = (J + 31) / 32;
+  const int j0 = lane * per;
+  int32_t *tp = plan + 4;
+  int32_t *sp = tp + (J + 1);
+  int32_t *lo_a = sp + (J + 1);
+  int32_t *hi_a = lo_a + (J + 1);
+  int t[8], local = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int j = j0 + k;
+    t[k] = 0;
+    if (k < per && j < J) {
+      const int bi = j / HG;
+      const int b = bi / q_len, i = bi % q_len;
+      int len = seq_lens[b];
+      if (len < 0 || len > max_blocks * kPage) {
+        if ((j % (q_len * HG)) == 0) raise_error(err, MLA_DEVERR_SEQ_LEN);
+        len = min(max(len, 0), max_blocks * kPage);
+      }
+      int hi = causal ? len - q_len + i + 1 : len;
+      hi = min(hi, len);
+      int lo = 0;
+      if (kv_starts) lo = max(lo, kv_starts[b]);
+      if (kv_ends) hi = min(hi, kv_ends[b]);
+      hi = max(hi, 0);
+      lo = min(max(lo, 0), hi);
+      lo_a[j] = lo;
+      hi_a[j] = hi;
+      t[k] = hi > lo ? (hi + tile - 1) / tile - lo / tile : 0;
+      local += t[k];
+    }
+  }
+  // exclusive scan of the lanes' sums; `tot` gets the warp total
+  auto excl_scan = [&](int v, int &tot) {
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    tot = __shfl_sync(0xffffffffu, x, 31);
+    return x - v;
+  };
+  int total;
+  int run = excl_scan(local, total);
+  int a[8];
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    a[k] = run;
+    if (k < per && j0 + k < J) tp[j0 + k] = run;
+    run += t[k];
+  }
+  const int C = forced_chunk > 0 ? forced_chunk : max(kMinTiles, (total + groups - 1) / groups);
+  int s[8];
+  local = 0;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int z = a[k] + t[k];
+    s[k] = (k < per && j0 + k < J && z > a[k]) ? (z - 1) / C - a[k] / C + 1 : 0;
+    local += s[k];
+  }
+  int segs;
+  run = excl_scan(local, segs);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    if (k < per && j0 + k < J) sp[j0 + k] = run;
+    run += s[k];
+  }
+  if (lane == 0) {
+    tp[J] = total;
+    sp[J] = segs;
+    lo_a[J] = 0;
+    hi_a[J] = 0;
+    plan[0] = total;
+    plan[1] = C;
+    plan[2] = J;
+    plan[3] = (total + C - 1) / C;
+  }
+}
+
+// Launches the plan on `stream` (one warp for small J), programmatic
+// stream serialization after the previous kernel.
+cudaError_t launch_plan(const int32_t *seq_lens, const int32_t *kv_starts, const int32_t *kv_ends,
+                        int B, int q_len, int HG, int max_blocks, int causal, int tile,
+                        int split_tiles, int groups, int32_t *plan, int *err,
+                        cudaStream_t stream) {
+  if (static_cast<int64_t>(B) * q_len * HG <= kWarpPlanJobs)
+    return launch_pdl(plan_warp_kernel, dim3(1), dim3(32), 0, stream, seq_lens, kv_starts,
+                      kv_ends, B, q_len, HG, max_blocks, causal, tile, split_tiles, groups,
+                      plan, err);
+  return launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, seq_lens, kv_starts,
+                    kv_ends, B, q_len, HG, max_blocks, causal, tile, split_tiles, groups, plan,
+                    err);
+}
+
 // ---------------------------------------------------------- segment walk
 struct Seg {
   int job, row0;        // job index, first q row ((b*q_len + i)*H + hg*128)
@@ -1718,9 +1830,8 @@ extern "C" int mla_decode_plan(const int32_t *seq_lens, const int32_t *kv_starts
   int *err = device_error_word();
   if (!err) return MLA_ERR_CUDA;
   const int tile = kv_dtype == MLA_E4M3 ? Geo<true>::kTile : Geo<false>::kTile;
-  if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, seq_lens, kv_starts,
-                 kv_ends, B, q_len, HG, max_blocks, causal ? 1 : 0, tile, split_tiles, g, plan,
-                 err) != cudaSuccess)
+  if (launch_plan(seq_lens, kv_starts, kv_ends, B, q_len, HG, max_blocks, causal ? 1 : 0, tile,
+                  split_tiles, g, plan, err, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
 }
@@ -1846,9 +1957,8 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   float *ws_lse = reinterpret_cast<float *>(ws + w.lse_off);
 
   const int tile = fp8 ? Geo<true>::kTile : Geo<false>::kTile;
-  if (launch_pdl(plan_kernel, dim3(1), dim3(kPlanThreads), 0, stream, seq_lens, kv_starts,
-                 kv_ends, B, q_len, HG, max_blocks, causal ? 1 : 0, tile, split_tiles, g, plan,
-                 err) != cudaSuccess)
+  if (launch_plan(seq_lens, kv_starts, kv_ends, B, q_len, HG, max_blocks, causal ? 1 : 0, tile,
+                  split_tiles, g, plan, err, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
 
   DecodeArgs a{};

@@ -113,6 +113,27 @@ def test_plan_matches_oracle(m, split_tiles, n_groups, fp8):
     assert np.array_equal(plan[4 + 3 * (J + 1):4 + 3 * (J + 1) + J], hi)
 
 
+def test_plan_matches_oracle_many_jobs(m):
+    """J = 400 jobs: beyond the one-warp plan, the block-scan plan kernel."""
+    g = synth.generator(431)
+    B, q_len, H = 200, 2, 128
+    seq = g.integers(0, 5000, B).astype(np.int32)
+    plan = m.mla_decode_plan(_i32(seq), B, q_len, H, 80, causal=True, n_groups=76).cpu().numpy()
+    lo, hi = [], []
+    for b in range(B):
+        for i in range(q_len):
+            a, z = O.decode_range(int(seq[b]), q_len, i, True, None, None)
+            lo.append(a)
+            hi.append(z)
+    ref = O.decode_plan(lo, hi, 76, tile=64, min_tiles=4)
+    J = len(lo)
+    assert plan[2] == J and plan[0] == ref["total"] and plan[1] == ref["chunk"]
+    assert np.array_equal(plan[4:4 + J + 1], ref["tile_prefix"])
+    assert np.array_equal(plan[4 + J + 1:4 + 2 * (J + 1)], ref["seg_prefix"])
+    assert np.array_equal(plan[4 + 2 * (J + 1):4 + 2 * (J + 1) + J], lo)
+    assert np.array_equal(plan[4 + 3 * (J + 1):4 + 3 * (J + 1) + J], hi)
+
+
 # ---------------------------------------------------------------- decode
 def _oracle_decode(case, kv_starts=None, kv_ends=None, causal=None):
     q = f64(case.q) * case.q_scale
