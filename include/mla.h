@@ -171,14 +171,16 @@ int mla_decode_paged_noalloc(const void *q, int q_dtype, float q_scale,
 /* A3 on its own: writes the split plan that mla_decode_paged computes.
  * Jobs are (b, i, head group of 128) in that nesting order; with the tile
  * size tk = 64 tokens (both kv dtypes; kv_dtype is kept so the tile may
- * differ by format), job j covers key tiles [lo/tk, ceil(hi/tk)); tiles of
- * all jobs are
- * concatenated into one flat space of `total` tiles, and CTA group p owns
- * flat tiles [p*C, (p+1)*C) with C = split_tiles if > 0, else
- * max(4, ceil(total / n_groups)).
+ * differ by format), job j covers key tiles [lo/tk, ceil(hi/tk)); the jobs
+ * are concatenated into one flat space where a non-empty job takes 4 units
+ * (the cost of switching a CTA pair to it, in tile-equivalents, no keys)
+ * followed by its tiles, `total` units in all, and CTA group p owns units
+ * [p*C, (p+1)*C) with C = split_tiles if > 0, else
+ * max(4, ceil(total / n_groups)), i.e. the tiles of every job it meets.
  * plan [4 + 4*(J+1)] int32 receives: [0] total, [1] C, [2] J, [3] number
- * of spans, then tile_prefix[J+1], seg_prefix[J+1] (partial results per
- * job, prefix-summed), job_lo[J+1], job_hi[J+1] (last entries 0).
+ * of spans, then unit_prefix[J+1] (units per job, prefix-summed),
+ * seg_prefix[J+1] (partial results per job, prefix-summed), job_lo[J+1],
+ * job_hi[J+1] (last entries 0).
  * n_groups = 0 uses half the device's SM count. */
 int mla_decode_plan(const int32_t *seq_lens, const int32_t *kv_starts,
                     const int32_t *kv_ends, int B, int q_len, int H,

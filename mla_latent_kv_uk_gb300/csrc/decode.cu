@@ -49,6 +49,12 @@ using namespace sm100;
 
 constexpr int kThreads = 192;
 constexpr int kMinTiles = 4;                 // smallest auto span
+// Units of the flat split space a non-empty job takes on top of its tiles:
+// switching a CTA pair to a job costs its epilogue and query load, measured
+// at about four 64-token tiles, so a span that meets a job start is given
+// that many fewer tiles and spans that cross request boundaries end with
+// the others.
+constexpr int kJobCost = 4;
 constexpr float kRescaleLog2 = 8.f;          // lazy rescale threshold
 constexpr uint32_t kColO = 0, kColS = 256;   // TMEM columns (both variants)
 
@@ -85,8 +91,9 @@ constexpr int smem_bytes() {
 }
 
 // ----------------------------------------------------------------- planner
-// Plan layout (int32): [0] total tiles, [1] C, [2] J, [3] spans, then
-// tile_prefix[J+1], seg_prefix[J+1], job_lo[J+1], job_hi[J+1].
+// Plan layout (int32): [0] total units, [1] C, [2] J, [3] spans, then
+// tile_prefix[J+1] (prefix of the units per job: its tiles + kJobCost, 0
+// for an empty job), seg_prefix[J+1], job_lo[J+1], job_hi[J+1].
 struct PlanView {
   const int32_t *base;
   int J;
@@ -175,7 +182,7 @@ plan_kernel(const int32_t *__restrict__ seq_lens,
     lo = min(max(lo, 0), hi);
     lo_a[j] = lo;
     hi_a[j] = hi;
-    tp[j] = hi > lo ? (hi + tile - 1) / tile - lo / tile : 0;
+    tp[j] = hi > lo ? (hi + tile - 1) / tile - lo / tile + kJobCost : 0;
   }
   if (threadIdx.x == 0) { lo_a[J] = 0; hi_a[J] = 0; }
   __syncthreads();
@@ -185,7 +192,8 @@ plan_kernel(const int32_t *__restrict__ seq_lens,
                                  : max(kMinTiles, (total + groups - 1) / groups);
   __syncthreads();
   for (int j = threadIdx.x; j < J; j += blockDim.x) {
-    const int a = tp[j], z = tp[j + 1];
+    const int z = tp[j + 1];
+    const int a = tp[j] + (z > tp[j] ? kJobCost : 0);   // the job's first tile
     sp[j] = z > a ? (z - 1) / C - a / C + 1 : 0;
   }
   __syncthreads();
@@ -244,7 +252,7 @@ plan_warp_kernel(const int32_t *__restrict__ seq_lens,
       lo = min(max(lo, 0), hi);
       lo_a[j] = lo;
       hi_a[j] = hi;
-      t[k] = hi > lo ? (hi + tile - 1) / tile - lo / tile : 0;
+      t[k] = hi > lo ? (hi + tile - 1) / tile - lo / tile + kJobCost : 0;
       local += t[k];
     }
   }
@@ -274,7 +282,8 @@ plan_warp_kernel(const int32_t *__restrict__ seq_lens,
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     const int z = a[k] + t[k];
-    s[k] = (k < per && j0 + k < J && z > a[k]) ? (z - 1) / C - a[k] / C + 1 : 0;
+    const int first = a[k] + (t[k] > 0 ? kJobCost : 0);   // the job's first tile
+    s[k] = (k < per && j0 + k < J && z > first) ? (z - 1) / C - first / C + 1 : 0;
     local += s[k];
   }
   int segs;
@@ -359,9 +368,11 @@ struct SegWalk {
         started = false;
         continue;
       }
-      const int a = tp[j], z = tp[j + 1];
-      if (z <= a) { ++j; continue; }  // empty job
+      const int z = tp[j + 1];
+      if (z <= tp[j]) { ++j; continue; }  // empty job
+      const int a = tp[j] + kJobCost;     // the job's first tile (after its switch cost)
       const int u0 = max(span_lo, a), u1 = min(span_hi, z);
+      if (u1 <= u0) { ++j; continue; }    // the span meets only the switch cost
       s.job = j;
       const int bi = j / HG, hg = j % HG;
       s.b = bi / q_len;
@@ -1730,7 +1741,7 @@ WsLayout ws_layout(int B, int q_len, int H, int max_seq_len, int split_tiles,
   const int HG = (H + 127) / 128;
   const int64_t J = static_cast<int64_t>(B) * q_len * HG;
   // bound with the smaller (bf16) tile: at least as many tiles as e4m3's
-  const int64_t tiles_per_job = (static_cast<int64_t>(max_seq_len) + 31) / 32 + 1;
+  const int64_t tiles_per_job = (static_cast<int64_t>(max_seq_len) + 31) / 32 + 1 + kJobCost;
   const int64_t total_max = J * tiles_per_job;
   const int64_t spans = split_tiles > 0 ? (total_max + split_tiles - 1) / split_tiles
                                         : static_cast<int64_t>(groups);

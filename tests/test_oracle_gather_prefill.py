@@ -91,30 +91,34 @@ def test_shard_local_index_is_a_bijection():
 
 
 @pytest.mark.parametrize("n_ctas", [1, 7, 152])
-def test_plan_covers_each_job_exactly_once(n_ctas):
+@pytest.mark.parametrize("job_cost", [0, 4])
+def test_plan_covers_each_job_exactly_once(n_ctas, job_cost):
     g = _rng(40)
     lo = g.integers(0, 50, 30)
     hi = lo + g.integers(0, 3000, 30)
     hi[3] = lo[3]                     # an empty job
-    plan = mla.decode_plan(lo, hi, n_ctas)
+    plan = mla.decode_plan(lo, hi, n_ctas, job_cost=job_cost)
     C, tp = plan["chunk"], plan["tile_prefix"]
     assert C >= -(-plan["total"] // n_ctas)
-    # brute force: walk every CTA's span and record segments per job
+    # brute force: walk every CTA's span and record which tiles of which job
+    # it meets; every tile of every job must be met exactly once
+    n = np.array([0 if hi[j] <= lo[j] else
+                  len(set(range(lo[j] // 32, (hi[j] - 1) // 32 + 1))) for j in range(len(lo))])
+    first = tp[:-1] + np.where(n > 0, job_cost, 0)
     segs = np.zeros(len(lo), np.int64)
-    seen = np.zeros(plan["total"], np.int64)
+    seen = [np.zeros(int(k), np.int64) for k in n]
     for p in range(-(-plan["total"] // C)):
         a, z = p * C, min((p + 1) * C, plan["total"])
-        seen[a:z] += 1
         for j in range(len(lo)):
-            if max(a, tp[j]) < min(z, tp[j + 1]):
+            u0, u1 = max(a, first[j]), min(z, tp[j + 1])
+            if u0 < u1:
                 segs[j] += 1
-    assert np.all(seen == 1)
+                seen[j][u0 - first[j]:u1 - first[j]] += 1
+    assert all(np.all(s_ == 1) for s_ in seen)
     assert np.array_equal(np.diff(plan["seg_prefix"]), segs)
     assert -(-plan["total"] // C) <= n_ctas
-    # per-job tile counts: tiles of 32 that meet [lo, hi)
-    for j in range(len(lo)):
-        n = 0 if hi[j] <= lo[j] else len(set(range(lo[j] // 32, (hi[j] - 1) // 32 + 1)))
-        assert tp[j + 1] - tp[j] == n
+    # units per job: its tiles of 32 that meet [lo, hi), plus the switch cost
+    assert np.array_equal(np.diff(tp), np.where(n > 0, n + job_cost, 0))
 
 
 def test_expand_brute_force():

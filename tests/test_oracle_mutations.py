@@ -109,7 +109,7 @@ def test_plan_segment_count_off_by_one(monkeypatch):
         r["seg_prefix"] = sp
         return r
     monkeypatch.setattr(O, "decode_plan", bad)
-    assert _fails(lambda: G.test_plan_covers_each_job_exactly_once(7))
+    assert _fails(lambda: G.test_plan_covers_each_job_exactly_once(7, 4))
 
 
 def test_prefill_causal_shift(monkeypatch):
