@@ -1707,28 +1707,122 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
 }
 
 // Combines the partials of every job cut into several spans; writes zeros
-// and -inf for jobs with an empty key range.  One warp per (job, head row).
+// and -inf for jobs with an empty key range.  One CTA per (job, 16-row
+// block): the 16 rows of one partial are contiguous (32 KB), so each part
+// is one bulk copy, with its 16 LSEs, into a 3-deep shared-memory ring (two
+// CTAs per SM keep ~190 KB of partials in flight).  Thread t owns row t/16
+// and the float4 columns (t%16) + 16k, k < 8 (conflict-free shared reads,
+// 128-byte output runs), and folds the parts in with an online rescale, so
+// any number of parts works.
+namespace mrg {
+constexpr int kRows = 16;
+constexpr int kRing = 3;
+constexpr int kPartFloats = kRows * kLatent;
+constexpr int kPartBytes = kPartFloats * 4;      // 32 KB
+constexpr int kLseBytes = kRows * 4;
+constexpr int kOffLse = kRing * kPartBytes;
+constexpr int kOffBars = kOffLse + kRing * kLseBytes;
+constexpr int kSmem = kOffBars + kRing * 8 + 16 + 128;
+}  // namespace mrg
+
 template <typename Tout>
-__global__ void __launch_bounds__(256)
+__global__ void __launch_bounds__(256, 2)
 decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
                     const float *__restrict__ ws_o,
-                    const float *__restrict__ ws_lse, Tout *out, float *lse) {
+                    const float *__restrict__ ws_lse, Tout *out, float *lse, int *err) {
+  using namespace mrg;
+  extern __shared__ __align__(128) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
+  float *parts = reinterpret_cast<float *>(smem);
+  const float *lses = reinterpret_cast<const float *>(smem + kOffLse);
+  uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBars);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kRing);
   sm100::grid_dep_wait();   // partials of the decode grid
   sm100::grid_dep_launch();
-  const int row = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int j = row >> 7, r = row & 127;
+  const int j = blockIdx.x / (128 / kRows), rb = blockIdx.x % (128 / kRows);
   if (j >= J) return;
   const int hg = j % HG;
-  if (hg * 128 + r >= H) return;
+  if (rb * kRows >= H - hg * 128) return;   // the whole block is past the head count
   const int32_t *sp = plan + 4 + (J + 1);
   const int s0 = sp[j], nseg = sp[j + 1] - s0;
   if (nseg == 1) return;  // written directly by the decode kernel
+  const int t = threadIdx.x, lr = t >> 4, q0 = t & 15;
+  const int r = rb * kRows + lr;
+  float acc[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) acc[k] = 0.f;
+  float m = -INFINITY, z = 0.f;
+  if (nseg > 0) {
+    if (t == 0) {
+      for (int b = 0; b < kRing; ++b) mbar_init(&full[b], 1);
+      *abort_flag = 0;
+      fence_barrier_init();
+    }
+    __syncthreads();
+    int issued = 0;
+    auto issue = [&](int s) {   // thread 0
+      const int b = s % kRing;
+      const int64_t slot = s0 + s;
+      mbar_arrive_expect_tx(&full[b], kPartBytes + kLseBytes);
+      bulk_load(parts + b * kPartFloats, ws_o + (slot * 128 + rb * kRows) * kLatent, kPartBytes,
+                &full[b]);
+      bulk_load(smem + kOffLse + b * kLseBytes, ws_lse + slot * 128 + rb * kRows, kLseBytes,
+                &full[b]);
+      ++issued;
+    };
+    if (t == 0)
+      for (int s = 0; s < min(nseg, kRing); ++s) issue(s);
+    int s = 0;
+    for (; s < nseg; ++s) {
+      const int b = s % kRing;
+      mbar_wait(&full[b], (s / kRing) & 1, abort_flag);
+      if (__syncthreads_or(*abort_flag != 0)) break;   // a timeout ends the loop for all
+      const float ls = lses[b * kRows + lr];
+      if (ls != -INFINITY) {   // an empty part (weight 0) is never folded in
+        const float mn = fmaxf(m, ls);
+        const float sc = expf(m - mn), w = expf(ls - mn);
+        z = z * sc + w;
+        m = mn;
+        const float4 *src = reinterpret_cast<const float4 *>(parts + b * kPartFloats + lr * kLatent);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float4 v = src[q0 + 16 * k];
+          acc[4 * k] = fmaf(w, v.x, acc[4 * k] * sc);
+          acc[4 * k + 1] = fmaf(w, v.y, acc[4 * k + 1] * sc);
+          acc[4 * k + 2] = fmaf(w, v.z, acc[4 * k + 2] * sc);
+          acc[4 * k + 3] = fmaf(w, v.w, acc[4 * k + 3] * sc);
+        }
+      }
+      __syncthreads();   // every thread has read buffer b
+      if (t == 0 && s + kRing < nseg) issue(s + kRing);
+    }
+    if (s < nseg) {
+      // timed out: the copies still in flight land before the CTA leaves
+      if (t == 0) {
+        volatile int no_abort = 0;
+        for (int u = s; u < issued; ++u) mbar_wait(&full[u % kRing], (u / kRing) & 1, &no_abort);
+        raise_error(err, MLA_DEVERR_TIMEOUT);
+      }
+      return;
+    }
+  }
+  if (hg * 128 + r >= H) return;
   const int64_t orow = static_cast<int64_t>(j / HG) * H + hg * 128 + r;
-  merge_row<float, Tout, 2>(ws_o + (static_cast<int64_t>(s0) * 128 + r) * kLatent,
-                         static_cast<int64_t>(128) * kLatent,
-                         ws_lse + static_cast<int64_t>(s0) * 128 + r, 128, nseg,
-                         kLatent, out + orow * kLatent, lse + orow,
-                         threadIdx.x & 31);
+  const float inv = m == -INFINITY ? 0.f : 1.f / z;
+  Tout *dst = out + orow * kLatent;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int c = 4 * (q0 + 16 * k);
+    const float a0 = acc[4 * k] * inv, a1 = acc[4 * k + 1] * inv, a2 = acc[4 * k + 2] * inv,
+                a3 = acc[4 * k + 3] * inv;
+    if constexpr (std::is_same<Tout, float>::value) {
+      *reinterpret_cast<float4 *>(dst + c) = make_float4(a0, a1, a2, a3);
+    } else {
+      *reinterpret_cast<uint2 *>(dst + c) = make_uint2(bf16x2_rn(a0, a1), bf16x2_rn(a2, a3));
+    }
+  }
+  if (q0 == 0) lse[orow] = m == -INFINITY ? -INFINITY : m + logf(z);
 }
 
 struct WsLayout {
@@ -1997,17 +2091,24 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
                                           stream);
   if (st != MLA_OK) return st;
 
-  const int64_t rows = static_cast<int64_t>(J) * 128;
-  const dim3 mgrid(static_cast<unsigned>((rows + 7) / 8));
+  const dim3 mgrid(static_cast<unsigned>(J) * (128 / mrg::kRows));
   const int32_t *cplan = plan;
   const float *cws_o = ws_o, *cws_lse = ws_lse;
   cudaError_t e;
-  if (out_dtype == MLA_BF16)
-    e = launch_pdl(decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(256), 0, stream, cplan,
-                   J, H, HG, cws_o, cws_lse, static_cast<__nv_bfloat16 *>(out), lse);
-  else
-    e = launch_pdl(decode_merge_kernel<float>, mgrid, dim3(256), 0, stream, cplan, J, H,
-                   HG, cws_o, cws_lse, static_cast<float *>(out), lse);
+  if (out_dtype == MLA_BF16) {
+    e = cudaFuncSetAttribute(decode_merge_kernel<__nv_bfloat16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, mrg::kSmem);
+    if (e == cudaSuccess)
+      e = launch_pdl(decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(256), mrg::kSmem, stream,
+                     cplan, J, H, HG, cws_o, cws_lse, static_cast<__nv_bfloat16 *>(out), lse,
+                     err);
+  } else {
+    e = cudaFuncSetAttribute(decode_merge_kernel<float>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, mrg::kSmem);
+    if (e == cudaSuccess)
+      e = launch_pdl(decode_merge_kernel<float>, mgrid, dim3(256), mrg::kSmem, stream, cplan, J,
+                     H, HG, cws_o, cws_lse, static_cast<float *>(out), lse, err);
+  }
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }
 
