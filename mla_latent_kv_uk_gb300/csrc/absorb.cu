@@ -72,14 +72,21 @@ __host__ __device__ inline uint32_t tmem_cols_for(int n) {
 }
 
 // ------------------------------------------------------------------ absorb
-// smem: A [2 K-chunks][4 l-blocks] of {64 l x 64 p} boxes (64 KB; once the
+// One CTA per (head, 128-wide latent block, token tile): four per head, so
+// the 16 MiB of weights spread over all SMs in 32 KB pieces and the work
+// left after a CTA's data lands (8 MMAs and one store) is short.
+constexpr int kAbsorbLat = 128;                       // latent columns per CTA
+constexpr int kAbsorbBlocks = kLatent / kAbsorbLat;   // CTAs per head
+constexpr int kAbsorbBoxes = 2 * kAbsorbLat / 64;     // W boxes: 2 K-chunks x l-blocks
+// smem: A [2 K-chunks][2 l-blocks] of {64 l x 64 p} boxes (32 KB; once the
 //       MMAs are done it stages the output), B [2 K-chunks] of {64 p x NT t}
-//       (NT * 128 B each), the q_pe tile {64 x NT t} (latent half 1 only;
-//       room for NT rounded up to 32 rows, as its chunks are stored whole).
+//       (NT * 128 B each), the q_pe tile {64 x NT t} (last latent block
+//       only; room for NT rounded up to 32 rows, as its chunks are stored
+//       whole).
 // The output leaves through tensor-map stores: per 32-token chunk one box
-// of this CTA's 256 latent columns and, for half 1, one of the 64 rope
-// columns (straight from the q_pe tile when the output is bf16).
-__global__ void __launch_bounds__(kThreads, 1)
+// of this CTA's 128 latent columns and, for the last block, one of the 64
+// rope columns (straight from the q_pe tile when the output is bf16).
+__global__ void __launch_bounds__(kThreads, 4)   // four CTAs (and their TMEM) per SM
 absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
               const __grid_constant__ CUtensorMap tm_q,
               const __grid_constant__ CUtensorMap tm_qpe,
@@ -89,8 +96,8 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int NT = args.NT;
-  uint8_t *sm_a = smem;                          // 64 KB
-  uint8_t *sm_b = smem + 8 * kBoxBytes64;        // 2 * NT * 128
+  uint8_t *sm_a = smem;                          // 32 KB
+  uint8_t *sm_b = smem + kAbsorbBoxes * kBoxBytes64;   // 2 * NT * 128
   uint8_t *sm_pe = sm_b + 2 * NT * 128;          // round_up(NT, 32) * 128
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm_pe + ((NT + 31) / 32) * 32 * 128);
   uint64_t *full = bars, *done = bars + 1, *drain = bars + 2;
@@ -99,7 +106,8 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
   volatile int *go = abort_flag + 1;             // the epilogue's common decision
 
   const int warp = warp_id(), lane = lane_id();
-  const int mh = blockIdx.x;          // latent half: l in [256 mh, 256 mh + 256)
+  const int mq = blockIdx.x;          // latent block: l in [128 mq, 128 mq + 128)
+  const bool rope = mq == kAbsorbBlocks - 1;   // this CTA also writes the rope columns
   const int h = blockIdx.y;
   const int t0 = blockIdx.z * NT;
   const int ntok = min(NT, args.T - t0);
@@ -113,7 +121,7 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, 2 * cols);
+    tmem_alloc(tmem_slot, cols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -128,14 +136,14 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_q);
-    mbar_arrive_expect_tx(full, 8 * kBoxBytes64 + 2 * NT * 128 + (mh == 1 ? NT * 128 : 0));
+    mbar_arrive_expect_tx(full, kAbsorbBoxes * kBoxBytes64 + 2 * NT * 128 + (rope ? NT * 128 : 0));
     for (int kc = 0; kc < 2; ++kc) {
-      for (int lb = 0; lb < 4; ++lb)   // W_UK_T as [H*128 rows (p), 512 cols (l)]
-        tma_load_2d(sm_a + (kc * 4 + lb) * kBoxBytes64, &tm_w, full,
-                    256 * mh + 64 * lb, h * 128 + 64 * kc);
+      for (int lb = 0; lb < 2; ++lb)   // W_UK_T as [H*128 rows (p), 512 cols (l)]
+        tma_load_2d(sm_a + (kc * 2 + lb) * kBoxBytes64, &tm_w, full,
+                    kAbsorbLat * mq + 64 * lb, h * 128 + 64 * kc);
       tma_load_3d(sm_b + kc * NT * 128, &tm_q, full, 64 * kc, h, t0);
     }
-    if (mh == 1) tma_load_3d(sm_pe, &tm_qpe, full, 0, h, t0);
+    if (rope) tma_load_3d(sm_pe, &tm_qpe, full, 0, h, t0);
     if (!mbar_wait(full, 0, abort_flag)) {
       volatile int no_abort = 0;
       mbar_wait(full, 0, &no_abort);
@@ -147,18 +155,16 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
       tc_fence_after();
       const uint32_t a = smem_u32(sm_a), b = smem_u32(sm_b);
 #pragma unroll
-      for (int mc = 0; mc < 2; ++mc)
+      for (int kc = 0; kc < 2; ++kc)
 #pragma unroll
-        for (int kc = 0; kc < 2; ++kc)
-#pragma unroll
-          for (int kk = 0; kk < 4; ++kk) {
-            // MN-major A: 128 B rows = 64 l of one p; 8-p groups 1024 B apart
-            // (SBO); the two 64-l blocks of this M chunk one box apart (LBO)
-            const uint64_t adesc = sdesc(a + (kc * 4 + 2 * mc) * kBoxBytes64 + kk * 2048,
-                                         kBoxBytes64, 1024, kSwizzle128B);
-            const uint64_t bdesc = sdesc(b + kc * NT * 128 + kk * 32, 16, 1024, kSwizzle128B);
-            mma_f16_ss(tmem + mc * cols, adesc, bdesc, idesc, (kc | kk) != 0);
-          }
+        for (int kk = 0; kk < 4; ++kk) {
+          // MN-major A: 128 B rows = 64 l of one p; 8-p groups 1024 B apart
+          // (SBO); the two 64-l blocks of the M = 128 block one box apart (LBO)
+          const uint64_t adesc = sdesc(a + kc * 2 * kBoxBytes64 + kk * 2048, kBoxBytes64, 1024,
+                                       kSwizzle128B);
+          const uint64_t bdesc = sdesc(b + kc * NT * 128 + kk * 32, 16, 1024, kSwizzle128B);
+          mma_f16_ss(tmem, adesc, bdesc, idesc, (kc | kk) != 0);
+        }
     }
     mma_commit(ok ? done : drain);
     if (!ok) {
@@ -168,7 +174,7 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
   } else if (warp >= 2) {
     const int tid = threadIdx.x - 64;
     const int quarter = warp & 3;
-    const int lrow = quarter * 32 + lane;       // latent row within an M chunk
+    const int lrow = quarter * 32 + lane;       // latent row within the block
     const int dt = args.out_dtype, es = esize(dt);
     mbar_wait(done, 0, abort_flag);
     // one decision for all four warps (a timed-out wait has set the flag
@@ -178,22 +184,22 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
     epi_bar();
     tc_fence_after();
     if (*go) {
-      // the MMAs have read A and B: A's 64 KB hold the staging
-      uint8_t *stg = sm_a;                      // [32 t][256 l] in the output dtype
-      uint8_t *stg_pe = sm_a + kStageTokens * 256 * 4;   // [32 t][64]
+      // the MMAs have read A and B: A's 32 KB hold the staging
+      uint8_t *stg = sm_a;                      // [32 t][128 l] in the output dtype
+      uint8_t *stg_pe = sm_a + kStageTokens * kAbsorbLat * 4;   // [32 t][64]
       for (int c0 = 0; c0 < ntok; c0 += kStageTokens) {
         if (c0 > 0) {   // the previous chunk's stores have read the staging
           if (tid == 0) bulk_wait_read_all();
           epi_bar();
         }
-        for (int mc = 0; mc < 2; ++mc) {
+        {
           uint32_t r[32];
-          tmem_ld_x32(tmem_addr(tmem, warp, mc * cols + c0), r);
+          tmem_ld_x32(tmem_addr(tmem, warp, c0), r);
 #pragma unroll
           for (int c = 0; c < 32; ++c)
-            put(stg + (c * 256 + mc * 128 + lrow) * es, dt, __uint_as_float(r[c]), args.q_scale);
+            put(stg + (c * kAbsorbLat + lrow) * es, dt, __uint_as_float(r[c]), args.q_scale);
         }
-        if (mh == 1 && dt != MLA_BF16) {
+        if (rope && dt != MLA_BF16) {
           // rope columns in the output dtype (bf16 leaves from its own tile)
           for (int i = tid; i < kStageTokens * 64; i += 128) {
             const int t = i >> 6, c = i & 63;
@@ -204,8 +210,8 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
         fence_proxy_async_smem();
         epi_bar();
         if (tid == 0) {
-          tma_store_3d(&tm_out, stg, 256 * mh, h, t0 + c0);
-          if (mh == 1)
+          tma_store_3d(&tm_out, stg, kAbsorbLat * mq, h, t0 + c0);
+          if (rope)
             tma_store_3d(&tm_out_pe, dt == MLA_BF16 ? sm_pe + c0 * 128 : stg_pe, kLatent, h,
                          t0 + c0);
         }
@@ -219,7 +225,7 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
   if (threadIdx.x == 0 && *abort_flag) raise_error(args.err, MLA_DEVERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * cols);
+    tmem_dealloc(tmem, cols);
   }
 }
 
@@ -409,7 +415,7 @@ extern "C" int mla_absorb_q(const void *q_nope, const void *q_pe,
     const uint64_t dims[3] = {static_cast<uint64_t>(kDqk), static_cast<uint64_t>(H),
                               static_cast<uint64_t>(T)};
     const uint64_t strides[2] = {kDqk * es, static_cast<uint64_t>(H) * kDqk * es};
-    const uint32_t box_lat[3] = {256, 1, static_cast<uint32_t>(kStageTokens)};
+    const uint32_t box_lat[3] = {kAbsorbLat, 1, static_cast<uint32_t>(kStageTokens)};
     const uint32_t box_pe[3] = {static_cast<uint32_t>(kRope), 1,
                                 static_cast<uint32_t>(kStageTokens)};
     if (!make_tmap(&to_lat, tdt, 3, q_out, dims, strides, box_lat, CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -418,11 +424,12 @@ extern "C" int mla_absorb_q(const void *q_nope, const void *q_pe,
   }
   GemmArgs a{T, H, NT, out_dtype, q_scale,
              static_cast<const __nv_bfloat16 *>(q_pe), q_out, err};
-  const size_t smem = 1024 + 8 * kBoxBytes64 + 2 * NT * 128 + ((NT + 31) / 32) * 32 * 128 + 64;
+  const size_t smem =
+      1024 + kAbsorbBoxes * kBoxBytes64 + 2 * NT * 128 + ((NT + 31) / 32) * 32 * 128 + 64;
   if (cudaFuncSetAttribute(absorb_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            static_cast<int>(smem)) != cudaSuccess)
     return MLA_ERR_CUDA;
-  dim3 grid(2, H, (T + NT - 1) / NT);
+  dim3 grid(kAbsorbBlocks, H, (T + NT - 1) / NT);
   if (launch_pdl(absorb_kernel, grid, dim3(kThreads), smem, stream, ta, tb, tpe, to_lat, to_pe,
                  a) != cudaSuccess)
     return MLA_ERR_CUDA;
