@@ -59,6 +59,15 @@ enum mla_device_error {
   MLA_DEVERR_TIMEOUT = 8,     /* a bounded wait inside a kernel gave up     */
 };
 
+/* Self-test of the failure detection every kernel relies on (no
+ * counterpart on the pages): one thread waits, through the same bounded
+ * mbarrier wait the kernels use, on a barrier that nothing completes; after
+ * limit_cycles SM cycles (1 .. 1e9) it gives up and raises
+ * MLA_DEVERR_TIMEOUT in the device error word, the way a kernel whose
+ * producer or peer stalls reports it.  Faults nothing, and the context stays
+ * usable.  MLA_ERR_INVALID_ARG for a limit out of range. */
+int mla_selftest_wait_timeout(long long limit_cycles, mla_stream_t stream);
+
 /* Human-readable text of a status code (static storage, never NULL). */
 const char *mla_status_string(int status);
 

@@ -19,7 +19,7 @@ from . import _build
 
 __all__ = [
     "MlaError", "BF16", "E4M3", "F32", "lib",
-    "mla_version", "mla_status_string", "mla_get_device_error",
+    "mla_version", "mla_status_string", "mla_get_device_error", "mla_selftest_wait_timeout",
     "mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
     "mla_decode_plan", "mla_merge_states", "mla_v_up", "mla_gather_cache",
     "mla_gather_cache_reorg", "mla_expand_kv", "mla_prefill_attn",
@@ -35,6 +35,7 @@ _SIGNATURES = {
     "mla_status_string": ([_i], ctypes.c_char_p),
     "mla_version": ([], _i),
     "mla_get_device_error": ([ctypes.POINTER(_i), _p], _i),
+    "mla_selftest_wait_timeout": ([ctypes.c_longlong, _p], _i),
     "mla_absorb_q": ([_p, _p, _p, _i, _i, _i, _f, _p, _p], _i),
     "mla_decode_workspace_size": ([_i, _i, _i, _i, _i, ctypes.POINTER(_sz)], _i),
     "mla_decode_paged": ([_p, _i, _f, _p, _i, _f, _p, _p, _p, _p, _i, _i, _i, _i,
@@ -114,6 +115,12 @@ def mla_get_device_error() -> int:
     code = _i(0)
     _check("mla_get_device_error", lib.mla_get_device_error(ctypes.byref(code), _stream()))
     return code.value
+
+
+def mla_selftest_wait_timeout(limit_cycles):
+    """Makes one bounded device wait run out (see include/mla.h)."""
+    _check("mla_selftest_wait_timeout",
+           lib.mla_selftest_wait_timeout(int(limit_cycles), _stream()))
 
 
 def mla_absorb_q(q_nope, q_pe, w_uk_t, out_dtype=torch.bfloat16, q_scale=1.0, out=None):

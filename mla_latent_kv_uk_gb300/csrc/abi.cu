@@ -1,10 +1,12 @@
 // Library-wide host plumbing: status strings, the device error word, the
-// per-device SM count and TMA descriptor encoding.
+// per-device SM count, TMA descriptor encoding, and the self-test of the
+// kernels' bounded waits.
 #include <cudaTypedefs.h>
 
 #include <mutex>
 
 #include "common.cuh"
+#include "sm100.cuh"
 
 namespace {
 
@@ -94,9 +96,30 @@ bool make_tmap(CUtensorMap *map, CUtensorMapDataType dtype, int rank,
   return r == CUDA_SUCCESS;
 }
 
+// One thread waits, through the kernels' bounded wait, on a barrier that
+// nothing completes; when the limit runs out it reports like every kernel.
+__global__ void selftest_wait_kernel(long long limit_cycles, int *err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  sm100::mbar_init(&bar, 1);
+  abort_flag = 0;
+  sm100::fence_barrier_init();
+  if (!sm100::mbar_wait_for(&bar, 0, &abort_flag, limit_cycles))
+    raise_error(err, MLA_DEVERR_TIMEOUT);
+}
+
 }  // namespace mla
 
 extern "C" {
+
+int mla_selftest_wait_timeout(long long limit_cycles, mla_stream_t stream) {
+  if (limit_cycles < 1 || limit_cycles > 1000000000LL) return MLA_ERR_INVALID_ARG;
+  int *err = mla::device_error_word();
+  if (!err) return MLA_ERR_CUDA;
+  mla::selftest_wait_kernel<<<1, 32, 0, stream>>>(limit_cycles, err);
+  return cudaGetLastError() == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
+}
 
 const char *mla_status_string(int status) {
   switch (status) {

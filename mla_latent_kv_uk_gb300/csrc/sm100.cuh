@@ -75,18 +75,23 @@ __device__ __forceinline__ bool mbar_test(uint64_t *bar, uint32_t parity) {
 // Bounded wait for the phase with `parity` to complete.  Returns false if
 // the CTA-wide abort flag is (or becomes) set, or the limit is reached, in
 // which case the flag is set so every other waiter gives up as well.
-__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
-                                          volatile int *abort_flag) {
+__device__ __forceinline__ bool mbar_wait_for(uint64_t *bar, uint32_t parity,
+                                              volatile int *abort_flag, long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitLimitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity,
+                                          volatile int *abort_flag) {
+  return mbar_wait_for(bar, parity, abort_flag, kWaitLimitCycles);
 }
 
 // --------------------------------------------------------------------- TMA

@@ -57,6 +57,9 @@ def test_host_validation_rejects_bad_arguments():
     import mla_latent_kv_uk_gb300 as m
     L = m.lib
     s = ctypes.c_void_p(0)
+    # bounded-wait self-test: the limit must be 1 .. 1e9 cycles
+    assert L.mla_selftest_wait_timeout(0, s) == 1
+    assert L.mla_selftest_wait_timeout(2 * 10 ** 9, s) == 1
     # merge: S = 0, D not a multiple of 8, bad dtype
     assert L.mla_merge_states(None, 0, None, 0, 1, 1, 8, None, 0, None, s) == 1
     assert L.mla_merge_states(None, 0, None, 2, 1, 1, 12, None, 0, None, s) == 1

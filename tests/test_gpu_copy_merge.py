@@ -134,3 +134,22 @@ def test_merge_states(m, S, T, H, D, pdt, odt):
     assert np.all(np.abs(f64(out) - ro) <= tol)
     d, finite = lse_close(lse.cpu().numpy(), rl, 1e-3)
     assert finite and d <= 1e-3
+
+
+def test_bounded_wait_timeout_is_reported_and_context_survives(m):
+    """Failure detection without a fault: a device wait on a barrier that
+    nothing completes gives up after ~1 ms of SM cycles and raises the
+    timeout bit; the context stays usable (a decode right after is correct
+    and raises nothing)."""
+    m.mla_get_device_error()                     # start from a clear word
+    m.mla_selftest_wait_timeout(2_000_000)
+    assert m.mla_get_device_error() & 8
+    case = synth.config1(poison=True)
+    out, lse = m.mla_decode_paged(
+        case.q.cuda(), case.cache.cuda(),
+        torch.as_tensor(case.block_table, dtype=torch.int32).cuda(),
+        torch.as_tensor(case.seq_lens, dtype=torch.int32).cuda(), sm_scale=case.sm_scale)
+    ref_o, _ = O.paged_decode(f64(case.q), f64(case.cache), case.block_table, case.seq_lens,
+                              case.sm_scale, causal=case.causal)
+    assert max_abs(f64(out), ref_o) <= 1e-2
+    assert m.mla_get_device_error() == 0
