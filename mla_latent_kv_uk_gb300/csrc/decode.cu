@@ -27,9 +27,11 @@
 //    epilogue.  Lazy rescaling: O is rescaled only when a row max grows by
 //    more than 2^8.
 //  * Work split (A3): every job (request, query token, 128-head group)
-//    contributes the 64-token tiles its key range touches; jobs are laid
-//    end to end and CTA pair p takes flat tiles [p*C, (p+1)*C).  A job cut
-//    into several spans writes fp32 partials that a merge kernel combines.
+//    contributes the 64-token tiles its key range touches, preceded by
+//    kJobCost units that stand for the cost of switching to it; jobs are
+//    laid end to end and CTA pair p takes units [p*C, (p+1)*C).  A job cut
+//    into several spans writes fp32 partials that a merge kernel combines
+//    (one CTA per 16 rows, partials streamed in by bulk copies).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <math.h>
@@ -920,7 +922,7 @@ constexpr int kStageBytes = 4 * kBox + kRopeBox;   // 36 KB
 constexpr int kPBuf = 128 * 128;                // 128 heads x 64 tokens bf16, SW128
 constexpr int kQRopeBytes = 128 * 64;           // 128 heads x 32 rope dims, SW64
 constexpr int kSMsg = 64 * 64 * 4;              // 64 rows x 64 fp32 scores
-constexpr int kAlMsg = 2 * 64 * 4;              // alpha[64], lq[64]
+constexpr int kAlMsg = 2 * 64 * 4;              // alpha[64], l[64]
 constexpr int kOffRing = 0;
 constexpr int kOffP = kOffRing + kStages * kStageBytes;       // [2] P operand tiles
 constexpr int kOffQ = kOffP + 2 * kPBuf;
