@@ -1046,6 +1046,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     }
     int kc = 0, nseg = 0;
     bool ok = true;
+    const uint64_t kv_policy = l2_evict_first_policy();
     // Publishes segment descriptor `ns` (or the end marker, ntiles = -1) in
     // the shared-memory ring read by the MMA thread and the softmax warps,
     // so they never walk the plan in global memory themselves.
@@ -1102,9 +1103,13 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           }
           uint8_t *dst = sm_kv + s * kStageBytes;
           mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
+          // the cache streams through once: its lines go first, so the query
+          // rows and the partials written for the merge stay in L2
           for (int j = 0; j < 4; ++j)
-            tma_load_2d(dst + j * kBox, &tm_kv, &kv_full[s], 256 * half + 64 * j, row);
-          tma_load_2d(dst + 4 * kBox, &tm_kr, &kv_full[s], kLatent + 32 * half, row);
+            tma_load_2d_hint(dst + j * kBox, &tm_kv, &kv_full[s], 256 * half + 64 * j, row,
+                             kv_policy);
+          tma_load_2d_hint(dst + 4 * kBox, &tm_kr, &kv_full[s], kLatent + 32 * half, row,
+                           kv_policy);
         }
         ++kc;
         return true;

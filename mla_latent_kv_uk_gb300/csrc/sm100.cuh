@@ -104,6 +104,23 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
       : "memory");
 }
 
+// L2 policy for data read once (evict it before anything else).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+
+// tma_load_2d with an L2 cache policy for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(void *dst, const CUtensorMap *map,
+                                                 uint64_t *bar, int x, int y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
 __device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map,
                                             uint64_t *bar, int x, int y,
                                             int z) {
