@@ -137,10 +137,13 @@ absorb_kernel(const __grid_constant__ CUtensorMap tm_w,
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_q);
     mbar_arrive_expect_tx(full, kAbsorbBoxes * kBoxBytes64 + 2 * NT * 128 + (rope ? NT * 128 : 0));
+    // the weights are read once per step: their lines leave L2 first, so
+    // the absorbed query written here is still there for the decode
+    const uint64_t w_policy = l2_evict_first_policy();
     for (int kc = 0; kc < 2; ++kc) {
       for (int lb = 0; lb < 2; ++lb)   // W_UK_T as [H*128 rows (p), 512 cols (l)]
-        tma_load_2d(sm_a + (kc * 2 + lb) * kBoxBytes64, &tm_w, full,
-                    kAbsorbLat * mq + 64 * lb, h * 128 + 64 * kc);
+        tma_load_2d_hint(sm_a + (kc * 2 + lb) * kBoxBytes64, &tm_w, full,
+                         kAbsorbLat * mq + 64 * lb, h * 128 + 64 * kc, w_policy);
       tma_load_3d(sm_b + kc * NT * 128, &tm_q, full, 64 * kc, h, t0);
     }
     if (rope) tma_load_3d(sm_pe, &tm_qpe, full, 0, h, t0);
@@ -279,12 +282,15 @@ vup_kernel(const __grid_constant__ CUtensorMap tm_w,
     prefetch_tmap(&tm_w);
     prefetch_tmap(&tm_o);
     int armed = -1;
+    // the weights are read once: their lines leave L2 before the latent
+    // output this kernel reads alongside them
+    const uint64_t w_policy = l2_evict_first_policy();
     for (int kc = 0; kc < KC; ++kc) {
       const int s = kc % stages;
       if (kc >= stages && !mbar_wait(&empty[s], ((kc / stages) - 1) & 1, abort_flag)) break;
       uint8_t *dst = smem + s * stage_bytes;
       mbar_arrive_expect_tx(&full[s], stage_bytes);
-      tma_load_2d(dst, &tm_w, &full[s], kc * 64, h * 128);  // W_UV [H*128 (v), 512 (l)]
+      tma_load_2d_hint(dst, &tm_w, &full[s], kc * 64, h * 128, w_policy);  // W_UV [H*128 (v), 512 (l)]
       tma_load_3d(dst + a_bytes, &tm_o, &full[s], kc * 64, h, t0);
       armed = kc;
     }
