@@ -248,6 +248,7 @@ def run_ours(args, rank, world, device):
     bytes_, flops, kv_tokens = algorithmic_counts(case.seq_lens, B, H)
     hbm, bf16, src = peaks()
     achieved = bytes_ / (ms_dec * 1e-3) / 1e9
+    traffic, traffic_src = decode_traffic()
     res = {
         "metric": METRIC, "value": whole_job_rate(B, world, ms), "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
@@ -259,8 +260,8 @@ def run_ours(args, rank, world, device):
         "e2e": {"value": whole_job_rate(B, world, ms_e2e), "unit": "tokens/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": ms_e2e},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                     "frac": achieved / hbm, "traffic": DECODE_TRAFFIC,
-                     "traffic_source": DECODE_TRAFFIC_SOURCE,
+                     "frac": achieved / hbm, "traffic": traffic,
+                     "traffic_source": traffic_src, "algorithmic_bytes": bytes_,
                      "kernel": "mla_decode_paged (plan + decode + merge launches)",
                      "kernel_ms": ms_dec, "peak_source": src,
                      "tensor_tflops": flops / (ms_dec * 1e-3) / 1e12,
@@ -273,14 +274,32 @@ def run_ours(args, rank, world, device):
     return res
 
 
-# DRAM bytes (read + write) of one decode_kernel launch on this workload, from
-# the ncu capture summarised in profiles/decode_pair_kernel_dsv3_b32_h128_ctx4096.md;
-# None whenever the kernel has changed since those counters were taken.
-# DRAM bytes per launch of the decode kernel from an ncu capture; None while
-# the kernel has changed since the last capture.
-DECODE_TRAFFIC = 159.43e6
-DECODE_TRAFFIC_SOURCE = ("ncu dram__bytes_read.sum + dram__bytes_write.sum, decode_pair_kernel, "
-                         "profiles/decode_pair_kernel_dsv3_b32_h128_ctx4096.md (bytes per launch)")
+# DRAM bytes (read + write) per launch of the decode kernel on this workload,
+# from one ncu capture (dram__bytes_read.sum + dram__bytes_write.sum), with
+# the SHA-256 of the kernel sources it was taken on: when the sources differ
+# the counters no longer describe the kernel and the line reports null.
+DECODE_TRAFFIC = {"bytes": None, "sources_sha256": None,
+                  "kernel": "decode_pair_kernel"}
+DECODE_SOURCES = ("decode.cu", "sm100.cuh", "common.cuh", "merge_row.cuh")
+
+
+def decode_sources_sha256():
+    import hashlib
+    h = hashlib.sha256()
+    for name in DECODE_SOURCES:
+        with open(os.path.join(ROOT, "mla_latent_kv_uk_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def decode_traffic():
+    """(bytes per launch or None, where the figure comes from)."""
+    if DECODE_TRAFFIC["bytes"] is None:
+        return None, "no ncu capture of the current kernel"
+    if DECODE_TRAFFIC["sources_sha256"] != decode_sources_sha256():
+        return None, "kernel changed since the ncu capture"
+    return DECODE_TRAFFIC["bytes"], ("ncu dram__bytes_read.sum + dram__bytes_write.sum, "
+                                     f"{DECODE_TRAFFIC['kernel']}, one launch")
 
 
 def oracle_sample(n_req):

@@ -153,19 +153,33 @@ int mla_decode_paged(const void *q, int q_dtype, float q_scale,
  * variant of A3/A4/A5.
  *
  * The plan and the split partials live in one static device array of
- * MLA_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library; every GPU that
- * loads the library holds it until the process exits.  Requests whose
- * workspace (mla_decode_workspace_size with max_seq_len = max_blocks*64)
- * exceeds that size are rejected with MLA_ERR_WORKSPACE.  The library never
- * allocates here: no cudaMalloc, cudaFree or allocating library routine.
- * The first call on a device looks the array's device address up once
- * (cudaGetSymbolAddress, with that device current) and caches it; make that
- * first call before any stream capture.  Every call shares the one array,
- * so calls that overlap on the GPU (different streams, or devices sharing a
- * context) race and must be serialised by the caller.  Nothing in the array
- * needs to start at zero: the plan is rewritten and every partial is
- * written before it is read on each call.  Arguments and results are those
- * of mla_decode_paged. */
+ * MLA_NOALLOC_SCRATCH_BYTES (64 MiB) inside the library.  Every GPU on
+ * which the library's decode module is loaded holds it until the process
+ * exits; with CUDA's default lazy module loading the 64 MiB is committed
+ * the first time the decode code is used on a device (the first decode
+ * call of any kind), so make that first call before device memory is
+ * carved up, and before any stream capture (it also looks the array's
+ * device address up once, with cudaGetSymbolAddress, and caches it per
+ * device index).  cudaDeviceReset is not supported once the library has
+ * been used: the cached address would belong to the old context.
+ *
+ * Size limit, in caller terms: the workspace is the plan plus one slot of
+ * 256.5 KB (a 128 x 512 fp32 partial and its 128 LSEs) for each of
+ * J + G partials, J = B * q_len * ceil(H / 128) jobs and G = the number of
+ * CTA pairs (76 on a 152-SM GB300) with the automatic split, or
+ * ceil(J * (max_blocks + 4) / split_tiles) with a forced
+ * split.  About 255 slots fit, so with the automatic split on a GB300 up
+ * to about 179 jobs run: the DeepSeek-V3 decode shape (B = 32, q_len 1,
+ * H = 128, J = 32) and B = 64 fp8 decode (J = 64) fit; B = 128 with
+ * q_len = 2 (J = 256) is rejected.  Larger requests return
+ * MLA_ERR_WORKSPACE, after every argument check of mla_decode_paged (a
+ * bad argument still returns MLA_ERR_INVALID_ARG).
+ * The library never allocates here: no cudaMalloc, cudaFree or allocating
+ * library routine.  Every call shares the one array, so calls that overlap
+ * on the GPU (different streams, or devices sharing a context) race and
+ * must be serialised by the caller.  Nothing in the array needs to start at
+ * zero: the plan is rewritten and every partial is written before it is
+ * read on each call.  Arguments and results are those of mla_decode_paged. */
 #define MLA_NOALLOC_SCRATCH_BYTES (64u * 1024u * 1024u)
 
 int mla_decode_paged_noalloc(const void *q, int q_dtype, float q_scale,

@@ -1841,8 +1841,10 @@ WsLayout ws_layout(int B, int q_len, int H, int max_seq_len, int split_tiles,
                    int groups) {
   const int HG = (H + 127) / 128;
   const int64_t J = static_cast<int64_t>(B) * q_len * HG;
-  // bound with the smaller (bf16) tile: at least as many tiles as e4m3's
-  const int64_t tiles_per_job = (static_cast<int64_t>(max_seq_len) + 31) / 32 + 1 + kJobCost;
+  // a job's key range [lo, hi) with 0 <= lo <= hi <= max_seq_len touches
+  // ceil(hi / tile) - floor(lo / tile) <= ceil(max_seq_len / tile) tiles
+  // (64 tokens for both formats), plus its switch cost in units
+  const int64_t tiles_per_job = (static_cast<int64_t>(max_seq_len) + 63) / 64 + kJobCost;
   const int64_t total_max = J * tiles_per_job;
   const int64_t spans = split_tiles > 0 ? (total_max + split_tiles - 1) / split_tiles
                                         : static_cast<int64_t>(groups);
@@ -2028,17 +2030,15 @@ int launch_decode_pair(const void *q, const void *kv_cache, int B, int q_len, in
 
 }  // namespace
 
-extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
-                                const void *kv_cache, int kv_dtype,
-                                float k_scale, const int32_t *block_table,
-                                const int32_t *seq_lens,
-                                const int32_t *kv_starts,
-                                const int32_t *kv_ends, int B, int q_len,
-                                int H, int max_blocks, int num_blocks,
-                                float sm_scale, int causal, int split_tiles,
-                                void *out, int out_dtype, float *lse,
-                                void *workspace, size_t ws_bytes,
-                                mla_stream_t stream) {
+namespace {
+
+// Host-side validation shared by mla_decode_paged and its no-allocation
+// variant: everything but the workspace.
+int validate_decode(const void *q, int q_dtype, float q_scale, const void *kv_cache,
+                    int kv_dtype, float k_scale, const int32_t *block_table,
+                    const int32_t *seq_lens, int B, int q_len, int H, int max_blocks,
+                    int num_blocks, float sm_scale, int split_tiles, const void *out,
+                    int out_dtype, const float *lse) {
   if (!decode_shape_ok(B, q_len, H) || max_blocks < 1 || num_blocks < 1 ||
       num_blocks >= (1 << 25) || split_tiles < 0)
     return MLA_ERR_INVALID_ARG;
@@ -2050,12 +2050,32 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
     return MLA_ERR_INVALID_ARG;
   if (out_dtype != MLA_BF16 && out_dtype != MLA_F32) return MLA_ERR_INVALID_ARG;
   if (!(sm_scale > 0.f) || !(sm_scale < INFINITY)) return MLA_ERR_INVALID_ARG;
+  if (kv_dtype == MLA_E4M3 && (!(q_scale > 0.f) || !(q_scale < INFINITY) ||
+                               !(k_scale > 0.f) || !(k_scale < INFINITY)))
+    return MLA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out)) return MLA_ERR_INVALID_ARG;
+  return MLA_OK;
+}
+
+}  // namespace
+
+extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
+                                const void *kv_cache, int kv_dtype,
+                                float k_scale, const int32_t *block_table,
+                                const int32_t *seq_lens,
+                                const int32_t *kv_starts,
+                                const int32_t *kv_ends, int B, int q_len,
+                                int H, int max_blocks, int num_blocks,
+                                float sm_scale, int causal, int split_tiles,
+                                void *out, int out_dtype, float *lse,
+                                void *workspace, size_t ws_bytes,
+                                mla_stream_t stream) {
+  const int v = validate_decode(q, q_dtype, q_scale, kv_cache, kv_dtype, k_scale, block_table,
+                                seq_lens, B, q_len, H, max_blocks, num_blocks, sm_scale,
+                                split_tiles, out, out_dtype, lse);
+  if (v != MLA_OK) return v;
+  if (!aligned16(workspace)) return MLA_ERR_INVALID_ARG;
   const bool fp8 = kv_dtype == MLA_E4M3;
-  if (fp8 && (!(q_scale > 0.f) || !(q_scale < INFINITY) || !(k_scale > 0.f) ||
-              !(k_scale < INFINITY)))
-    return MLA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(kv_cache) || !aligned16(out) || !aligned16(workspace))
-    return MLA_ERR_INVALID_ARG;
   const int g = groups_for_device();
   const WsLayout w = ws_layout(B, q_len, H, max_blocks * kPage, split_tiles, g);
   if (!workspace || ws_bytes < w.total) return MLA_ERR_WORKSPACE;
@@ -2150,9 +2170,11 @@ extern "C" int mla_decode_paged_noalloc(
     const int32_t *kv_starts, const int32_t *kv_ends, int B, int q_len, int H,
     int max_blocks, int num_blocks, float sm_scale, int causal, int split_tiles,
     void *out, int out_dtype, float *lse, mla_stream_t stream) {
-  if (!decode_shape_ok(B, q_len, H) || max_blocks < 1 || split_tiles < 0 ||
-      static_cast<int64_t>(max_blocks) * kPage > (1ll << 30))
-    return MLA_ERR_INVALID_ARG;
+  // every argument check of mla_decode_paged first, then the scratch size
+  const int v = validate_decode(q, q_dtype, q_scale, kv_cache, kv_dtype, k_scale, block_table,
+                                seq_lens, B, q_len, H, max_blocks, num_blocks, sm_scale,
+                                split_tiles, out, out_dtype, lse);
+  if (v != MLA_OK) return v;
   const WsLayout w = ws_layout(B, q_len, H, max_blocks * kPage, split_tiles,
                                groups_for_device());
   if (w.total > MLA_NOALLOC_SCRATCH_BYTES) return MLA_ERR_WORKSPACE;

@@ -173,46 +173,6 @@ def v_up(o_lat, w_uv):
 
 
 # --------------------------------------------------------------------------
-# A3: split-KV work plan (integer; the partition rule the kernels follow)
-# --------------------------------------------------------------------------
-
-def decode_plan(job_lo, job_hi, n_ctas, tile=32, min_tiles=4, forced_chunk=0, job_cost=4):
-    """Partition of every job's key tiles into contiguous per-CTA spans.
-
-    DCP + FP8 KV MLA decode digest, §关键源码片段 flashmla.py (the scheduler
-    metadata is derived from the true query-head count and seq_lens on the
-    device).  Rule (this library's): a job's key range [lo, hi) covers
-    absolute tiles [lo // tile, ceil(hi / tile)); jobs are concatenated in
-    order into one flat space where a non-empty job takes ``job_cost``
-    units (the cost of switching to it: its epilogue and query load, in
-    tile-equivalents; no keys) followed by its tiles, ``total`` units in
-    all; CTA group p owns units [p*C, (p+1)*C) with
-    C = max(min_tiles, ceil(total / n_ctas)), or C = forced_chunk when that
-    is > 0, and of them the tiles of every job they meet.
-    Returns dict(total, chunk, tile_prefix [J+1], seg_prefix [J+1]):
-    tile_prefix is the prefix of the units per job (tiles + job_cost, 0 for
-    an empty job), seg_prefix counts the spans that meet each job's tiles
-    (0 for empty jobs)."""
-    job_lo = np.asarray(job_lo, dtype=np.int64)
-    job_hi = np.asarray(job_hi, dtype=np.int64)
-    ntiles = np.where(job_hi > job_lo,
-                      (job_hi + tile - 1) // tile - job_lo // tile, 0)
-    units = np.where(ntiles > 0, ntiles + job_cost, 0)
-    tile_prefix = np.concatenate([[0], np.cumsum(units)])
-    total = int(tile_prefix[-1])
-    if forced_chunk > 0:
-        chunk = forced_chunk
-    else:
-        chunk = max(min_tiles, -(-total // n_ctas)) if total else min_tiles
-    first_tile = tile_prefix[:-1] + np.where(ntiles > 0, job_cost, 0)
-    segs = np.where(ntiles > 0,
-                    (tile_prefix[1:] - 1) // chunk - first_tile // chunk + 1, 0)
-    seg_prefix = np.concatenate([[0], np.cumsum(segs)])
-    return dict(total=total, chunk=chunk, tile_prefix=tile_prefix.astype(np.int64),
-                seg_prefix=seg_prefix.astype(np.int64))
-
-
-# --------------------------------------------------------------------------
 # A7: paged gather, dequantising gather, interleaved-shard reorg
 # --------------------------------------------------------------------------
 

@@ -1,5 +1,5 @@
 """GPU parity of the absorbed decode chain against the fp64 oracle:
-absorb (+ e4m3 concat-quant, bit-exact), v_up, the split plan (bit-exact)
+absorb (+ e4m3 concat-quant, bit-exact), v_up, the split plan (validity)
 and the paged decode with its on-device split merge."""
 
 import math
@@ -10,7 +10,9 @@ import torch
 
 import synth
 from oracle import codecs, mla as O
-from tests._helpers import bits, f64, gemm_tolerance, lse_close, max_abs
+from tests._helpers import (bits, check_attention, decode_terms, f64, gemm_tolerance, lse_close,
+                            max_abs, merge_bounds)
+from tests.plan_check import check_split_plan, job_ranges
 
 pytestmark = pytest.mark.gpu
 
@@ -79,10 +81,15 @@ def test_v_up(m, T, H):
 
 
 # ------------------------------------------------------------------ plan
+# The split plan is this library's schedule (the pages fix only that it is
+# derived on the device from seq_lens and the true head count), so the GPU
+# plan is checked for validity: every key tile of every job met by exactly
+# one span, consistent prefixes, no more spans than CTA groups, none longer
+# than C (tests/plan_check.py).
 @pytest.mark.parametrize("split_tiles,n_groups,fp8", [(0, 76, False), (3, 5, False),
                                                      (0, 1, False), (1, 2, False),
                                                      (0, 76, True), (2, 3, True)])
-def test_plan_matches_oracle(m, split_tiles, n_groups, fp8):
+def test_plan_is_valid(m, split_tiles, n_groups, fp8):
     g = synth.generator(430)
     B, q_len, H = 9, 2, 200
     seq = g.integers(0, 3000, B).astype(np.int32)
@@ -94,53 +101,47 @@ def test_plan_matches_oracle(m, split_tiles, n_groups, fp8):
                              n_groups=n_groups,
                              kv_dtype=torch.float8_e4m3fn if fp8 else torch.bfloat16
                              ).cpu().numpy()
-    HG = 2
-    lo, hi = [], []
-    for b in range(B):
-        for i in range(q_len):
-            for _ in range(HG):
-                a, z = O.decode_range(int(seq[b]), q_len, i, True, starts[b], ends[b])
-                lo.append(a)
-                hi.append(z)
-    ref = O.decode_plan(lo, hi, n_groups, tile=64, min_tiles=4,
-                        forced_chunk=split_tiles)
-    J = len(lo)
-    assert plan[2] == J
-    assert plan[0] == ref["total"] and plan[1] == ref["chunk"]
-    assert np.array_equal(plan[4:4 + J + 1], ref["tile_prefix"])
-    assert np.array_equal(plan[4 + J + 1:4 + 2 * (J + 1)], ref["seg_prefix"])
-    assert np.array_equal(plan[4 + 2 * (J + 1):4 + 2 * (J + 1) + J], lo)
-    assert np.array_equal(plan[4 + 3 * (J + 1):4 + 3 * (J + 1) + J], hi)
+    lo, hi = job_ranges(seq, q_len, H, True, starts, ends)
+    check_split_plan(plan, lo, hi, n_groups, split_tiles)
 
 
-def test_plan_matches_oracle_many_jobs(m):
-    """J = 400 jobs: beyond the one-warp plan, the block-scan plan kernel."""
-    g = synth.generator(431)
-    B, q_len, H = 200, 2, 128
+@pytest.mark.parametrize("B,q_len,n_groups", [(200, 2, 76), (32, 1, 76), (1, 1, 76),
+                                              (128, 2, 76)])
+def test_plan_is_valid_many_jobs(m, B, q_len, n_groups):
+    """Up to J = 400 jobs: the one-warp plan kernel (J <= 256) and the
+    block-scan plan kernel beyond it; the config-2 and config-5 shapes."""
+    g = synth.generator(431 + B)
+    H = 128
     seq = g.integers(0, 5000, B).astype(np.int32)
-    plan = m.mla_decode_plan(_i32(seq), B, q_len, H, 80, causal=True, n_groups=76).cpu().numpy()
-    lo, hi = [], []
-    for b in range(B):
-        for i in range(q_len):
-            a, z = O.decode_range(int(seq[b]), q_len, i, True, None, None)
-            lo.append(a)
-            hi.append(z)
-    ref = O.decode_plan(lo, hi, 76, tile=64, min_tiles=4)
-    J = len(lo)
-    assert plan[2] == J and plan[0] == ref["total"] and plan[1] == ref["chunk"]
-    assert np.array_equal(plan[4:4 + J + 1], ref["tile_prefix"])
-    assert np.array_equal(plan[4 + J + 1:4 + 2 * (J + 1)], ref["seg_prefix"])
-    assert np.array_equal(plan[4 + 2 * (J + 1):4 + 2 * (J + 1) + J], lo)
-    assert np.array_equal(plan[4 + 3 * (J + 1):4 + 3 * (J + 1) + J], hi)
+    plan = m.mla_decode_plan(_i32(seq), B, q_len, H, 80, causal=True,
+                             n_groups=n_groups).cpu().numpy()
+    lo, hi = job_ranges(seq, q_len, H, True)
+    check_split_plan(plan, lo, hi, n_groups)
 
 
 # ---------------------------------------------------------------- decode
-def _oracle_decode(case, kv_starts=None, kv_ends=None, causal=None):
+# Every decode check applies the north-star max-abs bounds (out 1e-2, LSE
+# 1e-3; fp8 KV out 5e-2) and the scale-aware elementwise bounds derived from
+# the kernel's roundings (tests/_helpers.py: bf16 output and P, e4m3 P on
+# the fp8 path, fp32 score accumulation); the helper prints the achieved
+# errors and their ratio to the bound.
+def _oracle_decode(case, kv_starts=None, kv_ends=None, causal=None, pick=None):
+    """(out, lse, error terms) of the oracle on the case's quantised inputs
+    (dequantised exactly), optionally for a subset of requests."""
     q = f64(case.q) * case.q_scale
     cache = f64(case.cache) * case.k_scale
-    return O.paged_decode(q, cache, case.block_table, case.seq_lens, case.sm_scale,
-                          causal=case.causal if causal is None else causal,
-                          kv_starts=kv_starts, kv_ends=kv_ends)
+    bt, sl = case.block_table, case.seq_lens
+    st, en = kv_starts, kv_ends
+    if pick is not None:
+        q, bt, sl = q[pick], bt[pick], sl[pick]
+        st = None if st is None else np.asarray(st)[pick]
+        en = None if en is None else np.asarray(en)[pick]
+    c = case.causal if causal is None else causal
+    ro, rl = O.paged_decode(q, cache, bt, sl, case.sm_scale, causal=c, kv_starts=st,
+                            kv_ends=en)
+    t = decode_terms(q, cache, bt, sl, case.sm_scale, causal=c, kv_starts=st, kv_ends=en,
+                     fp8=case.kv_dtype == "e4m3")
+    return ro, rl, t
 
 
 def _run_decode(m, case, split_tiles=0, out_dtype=torch.bfloat16, kv_starts=None,
@@ -154,19 +155,16 @@ def _run_decode(m, case, split_tiles=0, out_dtype=torch.bfloat16, kv_starts=None
         out_dtype=out_dtype)
 
 
-def _check(out, lse, ref_o, ref_l, out_tol=OUT_TOL, lse_tol=LSE_TOL):
-    d_o = max_abs(f64(out), ref_o)
-    d_l, finite = lse_close(lse.cpu().numpy(), ref_l, lse_tol)
-    assert finite, "NaN in LSE"
-    assert d_o <= out_tol, f"out max-abs {d_o}"
-    assert d_l <= lse_tol, f"lse max-abs {d_l}"
+def _check(out, lse, ro, rl, t, out_tol=OUT_TOL, lse_tol=LSE_TOL, label="decode"):
+    check_attention(f64(out).reshape(ro.shape), lse.cpu().numpy().reshape(rl.shape), ro, rl, t,
+                    out_tol=out_tol, lse_tol=lse_tol, out_bf16=out.dtype == torch.bfloat16,
+                    label=label)
 
 
 def test_decode_config1_tiny(m):
     case = synth.config1(poison=True)
     out, lse = _run_decode(m, case)
-    ro, rl = _oracle_decode(case)
-    _check(out, lse, ro, rl)
+    _check(out, lse, *_oracle_decode(case), label="config 1")
     assert m.mla_get_device_error() == 0
 
 
@@ -175,24 +173,21 @@ def test_decode_ragged_multi_tile(m, split_tiles):
     case = synth.decode_case("ragged", 440, B=4, H=128, seq_lens=[1, 33, 100, 1000],
                              poison=True)
     out, lse = _run_decode(m, case, split_tiles=split_tiles)
-    ro, rl = _oracle_decode(case)
-    _check(out, lse, ro, rl)
+    _check(out, lse, *_oracle_decode(case))
 
 
 def test_decode_fp32_out_and_head_groups(m):
     case = synth.decode_case("hg", 441, B=2, H=200, seq_lens=[77, 300], poison=True)
     out, lse = _run_decode(m, case, out_dtype=torch.float32, split_tiles=2)
-    ro, rl = _oracle_decode(case)
     # an fp32 output drops only the final bf16 rounding; P is still bf16
-    _check(out, lse, ro, rl)
+    _check(out, lse, *_oracle_decode(case))
 
 
 def test_decode_causal_pair(m):
     case = synth.decode_case("pair", 442, B=3, H=128, seq_lens=[2, 64, 513], q_len=2,
                              poison=True)
     out, lse = _run_decode(m, case, split_tiles=4)
-    ro, rl = _oracle_decode(case)
-    _check(out, lse, ro, rl)
+    _check(out, lse, *_oracle_decode(case))
 
 
 def test_decode_explicit_shards_then_merge(m):
@@ -205,21 +200,30 @@ def test_decode_explicit_shards_then_merge(m):
         st = np.array([sh[s][0] for sh in case.shards], np.int32)
         en = np.array([sh[s][1] for sh in case.shards], np.int32)
         o, l = _run_decode(m, case, kv_starts=st, kv_ends=en, out_dtype=torch.float32)
-        ro, rl = _oracle_decode(case, kv_starts=st, kv_ends=en)
-        _check(o, l, ro, rl, out_tol=1e-3)
+        _check(o, l, *_oracle_decode(case, kv_starts=st, kv_ends=en), out_tol=1e-3,
+               label=f"shard {s}")
         parts_o.append(o.reshape(B, case.H, 512))
         parts_l.append(l.reshape(B, case.H))
     mo, ml = m.mla_merge_states(torch.stack(parts_o), torch.stack(parts_l),
                                 out_dtype=torch.bfloat16)
-    ro, rl = _oracle_decode(case)
-    _check(mo, ml, ro.reshape(B, case.H, 512), rl.reshape(B, case.H))
+    # the merge on its own, against the oracle's merge of the GPU's own parts
+    po = np.stack([f64(x) for x in parts_o])
+    pl = np.stack([x.cpu().numpy().astype(np.float64) for x in parts_l])
+    mro, mrl = O.merge_states(po, pl)
+    bo, bl = merge_bounds(mro, mrl, po, pl)
+    assert np.all(np.abs(f64(mo) - mro) <= bo)
+    d, fin = lse_close(ml.cpu().numpy(), mrl, 1e-3)
+    assert fin and np.all(np.where(np.isneginf(mrl), 0.0, np.abs(ml.cpu().numpy() - mrl)) <= bl)
+    # and the whole split-and-merge against the unsplit oracle
+    ro, rl, t = _oracle_decode(case)
+    _check(mo, ml, ro.reshape(B, case.H, 512), rl.reshape(B, case.H),
+           t.take((slice(None), 0)), label="merged shards")
 
 
 def test_decode_empty_ranges(m):
     case = synth.decode_case("empty", 443, B=3, H=16, seq_lens=[0, 50, 50], poison=True)
     out, lse = _run_decode(m, case, kv_starts=[0, 20, 7], kv_ends=[0, 20, 9])
-    ro, rl = _oracle_decode(case, kv_starts=[0, 20, 7], kv_ends=[0, 20, 9])
-    _check(out, lse, ro, rl)
+    _check(out, lse, *_oracle_decode(case, kv_starts=[0, 20, 7], kv_ends=[0, 20, 9]))
     assert np.all(np.isneginf(lse.cpu().numpy()[:2]))
     assert np.all(f64(out)[:2] == 0)
 
@@ -230,10 +234,11 @@ def test_decode_peaked_scores(m):
     case = synth.decode_case("peaked", 444, B=2, H=128, seq_lens=[700, 2000], q_std=4.0,
                              kv_std_c=0.5, kv_std_pe=0.5, poison=True)
     out, lse = _run_decode(m, case)
-    ro, rl = _oracle_decode(case)
-    # outputs here reach |o| ~ 2; allow half a bf16 ulp on top of the budget
-    tol = OUT_TOL + 2.0 ** -8 * float(np.abs(ro).max())
-    _check(out, lse, ro, rl, out_tol=tol)
+    ro, rl, t = _oracle_decode(case)
+    # outputs reach |o| ~ 2, where the bf16 rounding of the output alone
+    # (half an ulp, 2^-8 relative) exceeds 1e-2: the max-abs bound gets that
+    # documented term; the elementwise bound is unchanged
+    _check(out, lse, ro, rl, t, out_tol=OUT_TOL + 2.0 ** -8 * float(np.abs(ro).max()))
 
 
 def test_chain_absorb_decode_vup_config2_sampled(m):
@@ -248,19 +253,21 @@ def test_chain_absorb_decode_vup_config2_sampled(m):
     pick = [0, 7, 19, 31]
     qo = f64(q)[pick]
     cache = f64(case.cache)
-    ro, rl = O.paged_decode(qo, cache, case.block_table[pick], case.seq_lens[pick],
-                            case.sm_scale)
-    _check(out[pick], lse[pick], ro, rl)
+    bt, sl = case.block_table[pick], case.seq_lens[pick]
+    # stage by stage: the decode against the oracle fed the GPU's own query
+    ro, rl = O.paged_decode(qo, cache, bt, sl, case.sm_scale)
+    t = decode_terms(qo, cache, bt, sl, case.sm_scale)
+    _check(out[pick], lse[pick], ro, rl, t, label="config 2 decode")
     ref_y = O.v_up(f64(out)[pick][:, 0], f64(case.w_uv))
     abs_sum = np.einsum("thl,hvl->thv", np.abs(f64(out)[pick][:, 0]), np.abs(f64(case.w_uv)))
     assert np.all(np.abs(f64(y)[pick] - ref_y) <= gemm_tolerance(ref_y, abs_sum))
-    # end-to-end against the unrounded fp64 chain
+    # end to end against the unrounded fp64 chain: the bf16 rounding of the
+    # absorbed query moves the exact LSE by (rl - el), computed here in fp64;
+    # beyond that shift the GPU stays within the benchmark spec's 1e-3
     q_true = O.absorb_q(f64(case.q_nope)[pick], f64(case.q_pe)[pick], f64(case.w_uk_t))
-    eo, el = O.paged_decode(q_true[:, None], cache, case.block_table[pick],
-                            case.seq_lens[pick], case.sm_scale)
+    eo, el = O.paged_decode(q_true[:, None], cache, bt, sl, case.sm_scale)
     assert max_abs(f64(out)[pick], eo) <= OUT_TOL
-    d, _ = lse_close(lse.cpu().numpy()[pick], el, LSE_TOL)
-    assert d <= 5 * LSE_TOL    # includes the bf16 rounding of the absorbed query
+    assert np.all(np.abs(lse.cpu().numpy()[pick] - el) <= LSE_TOL + np.abs(rl - el))
 
 
 def test_decode_config3_long_shards(m):
@@ -278,8 +285,9 @@ def test_decode_config3_long_shards(m):
                               kv_ends=_i32(en), out_dtype=torch.float32)
     mo, ml = m.mla_merge_states(o.view(S, 1, case.H, 512), l.view(S, 1, case.H),
                                 out_dtype=torch.bfloat16)
-    ro, rl = _oracle_decode(case)
-    _check(mo, ml, ro.reshape(1, case.H, 512), rl.reshape(1, case.H))
+    ro, rl, t = _oracle_decode(case)
+    _check(mo, ml, ro.reshape(1, case.H, 512), rl.reshape(1, case.H),
+           t.take((slice(None), 0)), label="config 3")
 
 
 def test_decode_config5_sampled(m):
@@ -288,10 +296,7 @@ def test_decode_config5_sampled(m):
     case = synth.config5_decode()
     out, lse = _run_decode(m, case)
     pick = [0, 1, 5, 17, 33, 50, 64, 77, 90, 101, 120, 127]
-    q = f64(case.q)[pick]
-    ro, rl = O.paged_decode(q, f64(case.cache), case.block_table[pick],
-                            case.seq_lens[pick], case.sm_scale, causal=True)
-    _check(out[pick], lse[pick], ro, rl)
+    _check(out[pick], lse[pick], *_oracle_decode(case, pick=pick), label="config 5 decode")
 
 
 def test_decode_reruns_bit_identical(m):
@@ -318,10 +323,10 @@ def test_decode_many_short_jobs(m):
     seq = g.integers(0, 200, B).astype(np.int32)
     case = synth.decode_case("many_jobs", 471, B=B, H=16, seq_lens=seq, q_len=2, poison=True)
     out, lse = _run_decode(m, case)
-    ro, rl = _oracle_decode(case)
-    # contexts of a few tokens leave outputs near single value rows (|out| up
-    # to ~4): bf16 rounding of P and of the output, 2^-9 each, relative
-    _check(out, lse, ro, rl, out_tol=OUT_TOL + 2.0 ** -8 * float(np.abs(ro).max()))
+    ro, rl, t = _oracle_decode(case)
+    # contexts of a few tokens leave outputs near single value rows (|out|
+    # up to ~4): the max-abs bound gets the bf16 half-ulp term of the output
+    _check(out, lse, ro, rl, t, out_tol=OUT_TOL + 2.0 ** -8 * float(np.abs(ro).max()))
     assert m.mla_get_device_error() == 0
 
 
@@ -334,8 +339,8 @@ def test_decode_fp8_ragged(m, split_tiles):
     case = synth.decode_case("fp8_small", 450, B=3, H=128, seq_lens=[5, 100, 700],
                              kv_dtype="e4m3", q_dtype="e4m3", poison=True)
     out, lse = _run_decode(m, case, split_tiles=split_tiles)
-    ro, rl = _oracle_decode(case)
-    _check(out, lse, ro, rl, out_tol=FP8_OUT_TOL, lse_tol=FP8_LSE_TOL)
+    _check(out, lse, *_oracle_decode(case), out_tol=FP8_OUT_TOL, lse_tol=FP8_LSE_TOL,
+           label="fp8 ragged")
     assert m.mla_get_device_error() == 0
 
 
@@ -343,8 +348,8 @@ def test_decode_fp8_causal_pair_head_groups(m):
     case = synth.decode_case("fp8_pair", 451, B=2, H=144, seq_lens=[70, 1000], q_len=2,
                              kv_dtype="e4m3", q_dtype="e4m3", poison=True)
     out, lse = _run_decode(m, case, out_dtype=torch.float32)
-    ro, rl = _oracle_decode(case)
-    _check(out, lse, ro, rl, out_tol=FP8_OUT_TOL, lse_tol=FP8_LSE_TOL)
+    _check(out, lse, *_oracle_decode(case), out_tol=FP8_OUT_TOL, lse_tol=FP8_LSE_TOL,
+           label="fp8 pair")
 
 
 def test_decode_config4_fp8_sampled(m):
@@ -353,7 +358,5 @@ def test_decode_config4_fp8_sampled(m):
     case = synth.config4()
     out, lse = _run_decode(m, case)
     pick = [0, 9, 21, 40, 52, 63]
-    q = f64(case.q)[pick] * case.q_scale
-    ro, rl = O.paged_decode(q, f64(case.cache) * case.k_scale, case.block_table[pick],
-                            case.seq_lens[pick], case.sm_scale)
-    _check(out[pick], lse[pick], ro, rl, out_tol=FP8_OUT_TOL, lse_tol=FP8_LSE_TOL)
+    _check(out[pick], lse[pick], *_oracle_decode(case, pick=pick), out_tol=FP8_OUT_TOL,
+           lse_tol=FP8_LSE_TOL, label="config 4")

@@ -9,7 +9,7 @@ import torch
 
 import synth
 from oracle import mla as O
-from tests._helpers import bits, f64, lse_close, max_abs
+from tests._helpers import bits, f64, lse_close, max_abs, merge_bounds
 
 pytestmark = pytest.mark.gpu
 
@@ -129,11 +129,15 @@ def test_merge_states(m, S, T, H, D, pdt, odt):
         po[:, 0, 1] = float("nan")              # whose parts hold NaN
     out, lse = m.mla_merge_states(po.cuda(), torch.from_numpy(pl).cuda(), out_dtype=odt)
     ro, rl = O.merge_states(f64(po), pl.astype(np.float64))
-    # fp32 arithmetic error plus, for a bf16 output, half an ulp of the result
-    tol = 1e-4 + (2.0 ** -8 * np.abs(ro) if odt == torch.bfloat16 else 0.0)
-    assert np.all(np.abs(f64(out) - ro) <= tol)
+    # output rounding plus the fp32 rescaling error (tests/_helpers.py)
+    bo, bl = merge_bounds(ro, rl, f64(po), pl, out_bf16=odt == torch.bfloat16)
+    err = np.abs(f64(out) - ro)
+    print(f"merge S={S}: out max-abs {err.max():.3e} ({(err / bo).max():.3f} of its bound)")
+    assert np.all(err <= bo)
     d, finite = lse_close(lse.cpu().numpy(), rl, 1e-3)
     assert finite and d <= 1e-3
+    gl = lse.cpu().numpy()
+    assert np.all(np.where(np.isneginf(rl), 0.0, np.abs(gl - rl)) <= bl)
 
 
 def test_bounded_wait_timeout_is_reported_and_context_survives(m):

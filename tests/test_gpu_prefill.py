@@ -9,7 +9,8 @@ import torch
 
 import synth
 from oracle import mla as O
-from tests._helpers import f64, gemm_tolerance, lse_close, max_abs
+from tests._helpers import (bits, check_attention, f64, gemm_tolerance, lse_close, max_abs,
+                            merge_bounds, prefill_terms)
 
 pytestmark = pytest.mark.gpu
 
@@ -56,9 +57,9 @@ def test_prefill_attention_small(m, causal):
     out, lse = m.mla_prefill_attn(q.cuda(), k.cuda(), v.cuda(), _i32(cu_q), _i32(cu_k),
                                   int(nq.max()), causal=causal, sm_scale=scale)
     ro, rl = O.prefill_attention(f64(q), f64(k), f64(v), cu_q, cu_k, causal, scale)
-    assert max_abs(f64(out), ro) <= OUT_TOL
-    d, fin = lse_close(lse.cpu().numpy(), rl, LSE_TOL)
-    assert fin and d <= LSE_TOL
+    t = prefill_terms(f64(q), f64(k), f64(v), cu_q, cu_k, causal, scale)
+    check_attention(f64(out), lse.cpu().numpy(), ro, rl, t, out_tol=OUT_TOL, lse_tol=LSE_TOL,
+                    label=f"prefill causal={causal}")
 
 
 def test_prefill_no_visible_keys(m):
@@ -75,14 +76,19 @@ def test_prefill_no_visible_keys(m):
                                   causal=True, sm_scale=0.1)
     ro, rl = O.prefill_attention(f64(q), f64(k), f64(v), cu_q, cu_k, True, 0.1)
     assert np.all(np.isneginf(lse.cpu().numpy()[:3])) and np.all(np.isneginf(rl[:3]))
-    assert max_abs(f64(out), ro) <= OUT_TOL
+    t = prefill_terms(f64(q), f64(k), f64(v), cu_q, cu_k, True, 0.1)
+    check_attention(f64(out), lse.cpu().numpy(), ro, rl, t, out_tol=OUT_TOL, lse_tol=LSE_TOL,
+                    label="no visible keys")
 
 
 def test_chunked_prefill_config5_sampled(m):
-    """Config 5 context step: 4 requests x 8192 context rows on 4 interleaved
-    shards, 512 new tokens each; gather+reorg -> expand -> non-causal context
-    attention; new tokens expand -> causal attention; LSE merge.  The oracle
-    checks 2 heads x 16 query rows per request (it expands only those heads)."""
+    """Config 5 context step at full size: 4 requests x 8192 context rows on
+    4 interleaved shards, 512 new tokens each, H = 128.  Stage by stage, each
+    against the oracle fed the GPU's own inputs to that stage: gather+reorg
+    (bit-exact), expand (GEMM bound), non-causal context attention and causal
+    new-token attention (spec and scale-aware bounds), LSE merge; then
+    end to end against the unrounded fp64 chain.  The oracle samples 2 heads
+    x 16 query rows per request (it expands only those heads)."""
     case = synth.config5_prefill()
     W, I, H = case.W, case.interleave, case.H
     ctx, new = case.ctx_lens, case.new_lens
@@ -108,21 +114,55 @@ def test_chunked_prefill_config5_sampled(m):
     out, lse = m.mla_merge_states(torch.stack([oc, on]), torch.stack([lc, ln]),
                                   out_dtype=torch.bfloat16)
     assert m.mla_get_device_error() == 0
-    # oracle on sampled heads / rows
+    assert Tq == 2048
     heads = [0, 77]
     g = synth.generator(530)
     q_rows = np.concatenate([cu_q[b] + np.sort(g.choice(new[b], 16, replace=False))
                              for b in range(case.B)])
-    ctx_rows = O.gather_cache(f64(case.cache), case.block_table, cu_c)
-    Kc, Vc = O.expand_kv(ctx_rows, f64(case.w_kvb), H, heads=heads)
-    Kn, Vn = O.expand_kv(f64(case.new_kv), f64(case.w_kvb), H, heads=heads)
     qs = f64(case.q)[:, heads]
-    ro, rl, merges = O.chunked_prefill(qs, Kn, Vn, Kc, Vc, cu_q, cu_c, case.sm_scale,
-                                       n_chunks=1, q_rows=q_rows)
+    sc = case.sm_scale
+    # gather + reorg: bit-exact
+    ctx_bits = O.gather_cache(bits(case.cache), case.block_table, cu_c)
+    assert np.array_equal(bits(rows), ctx_bits)
+    ctx_rows = O.gather_cache(f64(case.cache), case.block_table, cu_c)
+    # expand, sampled heads
+    Kc, Vc = O.expand_kv(ctx_rows, f64(case.w_kvb), H, heads=heads)
+    kc_s, vc_s = f64(kc[:, heads]), f64(vc[:, heads])
+    wabs = np.abs(f64(case.w_kvb)).reshape(H, 256, 512)[heads]
+    absk = np.einsum("nl,hcl->nhc", np.abs(ctx_rows[:, :512]), wabs)
+    assert np.all(np.abs(kc_s[..., :128] - Kc[..., :128]) <= gemm_tolerance(Kc[..., :128], absk[..., :128]))
+    assert np.array_equal(kc_s[..., 128:], Kc[..., 128:])
+    assert np.all(np.abs(vc_s - Vc) <= gemm_tolerance(Vc, absk[..., 128:]))
+    # context attention on the GPU's own K/V
+    roc, rlc = O.prefill_attention(qs, kc_s, vc_s, cu_q, cu_c, False, sc, q_rows)
+    tc = prefill_terms(qs, kc_s, vc_s, cu_q, cu_c, False, sc, q_rows)
+    check_attention(f64(oc[:, heads])[q_rows], lc[:, heads].cpu().numpy()[q_rows], roc[q_rows],
+                    rlc[q_rows], tc.take(q_rows), out_tol=OUT_TOL, lse_tol=LSE_TOL,
+                    label="config 5 context attention")
+    # new-token causal attention on the GPU's own K/V
+    kn_s, vn_s = f64(kn[:, heads]), f64(vn[:, heads])
+    ron, rln = O.prefill_attention(qs, kn_s, vn_s, cu_q, cu_q, True, sc, q_rows)
+    tn = prefill_terms(qs, kn_s, vn_s, cu_q, cu_q, True, sc, q_rows)
+    check_attention(f64(on[:, heads])[q_rows], ln[:, heads].cpu().numpy()[q_rows], ron[q_rows],
+                    rln[q_rows], tn.take(q_rows), out_tol=OUT_TOL, lse_tol=LSE_TOL,
+                    label="config 5 new-token attention")
+    # the merge of the GPU's own two states
+    po = np.stack([f64(oc[:, heads])[q_rows], f64(on[:, heads])[q_rows]])
+    pl = np.stack([lc[:, heads].cpu().numpy()[q_rows], ln[:, heads].cpu().numpy()[q_rows]])
+    mo, ml = O.merge_states(po, pl.astype(np.float64))
+    bo, bl = merge_bounds(mo, ml, po, pl)
+    got_o = f64(out[:, heads])[q_rows]
+    got_l = lse[:, heads].cpu().numpy()[q_rows].astype(np.float64)
+    assert np.all(np.abs(got_o - mo) <= bo)
+    assert np.all(np.abs(got_l - ml) <= bl)
+    # end to end against the unrounded chain: the bf16 rounding of the
+    # expanded K/V moves the exact result by (staged - unrounded), computed
+    # here in fp64; beyond that the GPU stays within the benchmark spec's bounds
+    Kn, Vn = O.expand_kv(f64(case.new_kv), f64(case.w_kvb), H, heads=heads)
+    eo, el, merges = O.chunked_prefill(qs, Kn, Vn, Kc, Vc, cu_q, cu_c, sc, n_chunks=1,
+                                       q_rows=q_rows)
     assert merges == 1
-    got_o = f64(out)[q_rows][:, heads]
-    got_l = lse.cpu().numpy()[q_rows][:, heads]
-    assert max_abs(got_o, ro[q_rows]) <= OUT_TOL
-    d, fin = lse_close(got_l, rl[q_rows], LSE_TOL)
-    assert fin and d <= 2 * LSE_TOL
-    assert Tq == 2048
+    so, sl = O.merge_states(np.stack([roc[q_rows], ron[q_rows]]),
+                            np.stack([rlc[q_rows], rln[q_rows]]))
+    assert max_abs(got_o, eo[q_rows]) <= OUT_TOL
+    assert np.all(np.abs(got_l - el[q_rows]) <= LSE_TOL + np.abs(sl - el[q_rows]))

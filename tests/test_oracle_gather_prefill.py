@@ -1,5 +1,5 @@
-"""Pins for the oracle's gather / dequant / reorg, split plan, expand and
-prefill-attention definitions."""
+"""Pins for the oracle's gather / dequant / reorg, expand and prefill-attention
+definitions, and for the split-plan validity checker."""
 
 import math
 
@@ -90,35 +90,55 @@ def test_shard_local_index_is_a_bijection():
             assert np.array_equal(jj, np.arange(len(jj)))
 
 
-@pytest.mark.parametrize("n_ctas", [1, 7, 152])
-@pytest.mark.parametrize("job_cost", [0, 4])
-def test_plan_covers_each_job_exactly_once(n_ctas, job_cost):
-    g = _rng(40)
-    lo = g.integers(0, 50, 30)
-    hi = lo + g.integers(0, 3000, 30)
-    hi[3] = lo[3]                     # an empty job
-    plan = mla.decode_plan(lo, hi, n_ctas, job_cost=job_cost)
-    C, tp = plan["chunk"], plan["tile_prefix"]
-    assert C >= -(-plan["total"] // n_ctas)
-    # brute force: walk every CTA's span and record which tiles of which job
-    # it meets; every tile of every job must be met exactly once
-    n = np.array([0 if hi[j] <= lo[j] else
-                  len(set(range(lo[j] // 32, (hi[j] - 1) // 32 + 1))) for j in range(len(lo))])
-    first = tp[:-1] + np.where(n > 0, job_cost, 0)
-    segs = np.zeros(len(lo), np.int64)
-    seen = [np.zeros(int(k), np.int64) for k in n]
-    for p in range(-(-plan["total"] // C)):
-        a, z = p * C, min((p + 1) * C, plan["total"])
-        for j in range(len(lo)):
-            u0, u1 = max(a, first[j]), min(z, tp[j + 1])
-            if u0 < u1:
-                segs[j] += 1
-                seen[j][u0 - first[j]:u1 - first[j]] += 1
-    assert all(np.all(s_ == 1) for s_ in seen)
-    assert np.array_equal(np.diff(plan["seg_prefix"]), segs)
-    assert -(-plan["total"] // C) <= n_ctas
-    # units per job: its tiles of 32 that meet [lo, hi), plus the switch cost
-    assert np.array_equal(np.diff(tp), np.where(n > 0, n + job_cost, 0))
+# The split plan is the library's own schedule, not a definition from the
+# pages, so it is checked for validity (tests/plan_check.py), not against a
+# reference schedule.  These pins make sure the checker accepts a plan worked
+# out by hand and rejects plausible corruptions of it.
+#   jobs: [0,130) -> key tiles 0..2 (3 tiles); [10,10) empty; [0,64) -> 1 tile
+#   units: 3 + 4 (switch cost), 0, 1 + 4  -> prefix 0, 7, 7, 12 (total 12)
+#   auto, 3 groups: C = 4, spans [0,4) [4,8) [8,12); job 0's tiles sit at
+#   units 4..6 (span 1 only), job 2's at unit 11 (span 2) -> segs 1, 0, 1
+#   forced C = 2: spans of 2 units; job 0 at 4..6 meets spans 2 and 3,
+#   job 2 at 11 meets span 5 -> segs 2, 0, 1
+_LO, _HI = [0, 10, 0], [130, 10, 64]
+_PLAN_AUTO3 = [12, 4, 3, 3, 0, 7, 7, 12, 0, 1, 1, 2, 0, 10, 0, 0, 130, 10, 64, 0]
+_PLAN_FORCED2 = [12, 2, 3, 6, 0, 7, 7, 12, 0, 2, 2, 3, 0, 10, 0, 0, 130, 10, 64, 0]
+
+
+def test_plan_checker_accepts_hand_worked_plans():
+    from tests.plan_check import check_split_plan
+    check_split_plan(_PLAN_AUTO3, _LO, _HI, n_groups=3)
+    check_split_plan(_PLAN_FORCED2, _LO, _HI, n_groups=3, split_tiles=2)
+
+
+@pytest.mark.parametrize("field,idx,value", [
+    ("seg", 11, 3),         # one extra segment counted for job 2
+    ("units", 1, 6),        # job 0 short of one tile (prefix 0, 6, 6, 11)
+    ("chunk", 1, 3),        # C = 3 -> 4 spans for 3 groups
+    ("hi", 16, 129),        # job 0's key range recorded wrong
+    ("spans", 3, 2),        # span count inconsistent with C
+])
+def test_plan_checker_rejects_corrupted_plans(field, idx, value):
+    from tests.plan_check import check_split_plan
+    plan = list(_PLAN_AUTO3)
+    if field == "units":
+        plan[4:8] = [0, 6, 6, 11]
+        plan[0] = 11
+    elif field == "chunk":
+        plan[1], plan[3] = 3, 4
+    else:
+        plan[idx] = value
+    with pytest.raises(AssertionError):
+        check_split_plan(plan, _LO, _HI, n_groups=3)
+
+
+def test_job_ranges_follow_the_causal_definition():
+    from tests.plan_check import job_ranges
+    lo, hi = job_ranges([5, 0], 2, 200, True, kv_starts=[1, 0], kv_ends=[4, 9])
+    # request 0: token 0 sees keys < 4 -> [1,4); token 1 < 5 -> [1, min(5,4)=4)
+    # request 1: empty; two head groups per (request, token)
+    assert lo.tolist() == [1, 1, 1, 1, 0, 0, 0, 0]
+    assert hi.tolist() == [4, 4, 4, 4, 0, 0, 0, 0]
 
 
 def test_expand_brute_force():

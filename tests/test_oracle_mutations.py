@@ -99,19 +99,6 @@ def test_gather_ignores_seq_starts(monkeypatch):
     assert _fails(G.test_gather_seq_starts_equals_slice_of_full_gather)
 
 
-def test_plan_segment_count_off_by_one(monkeypatch):
-    orig = O.decode_plan
-
-    def bad(*a, **k):
-        r = orig(*a, **k)
-        sp = r["seg_prefix"].copy()
-        sp[1:] += np.arange(1, len(sp))       # one extra segment per job
-        r["seg_prefix"] = sp
-        return r
-    monkeypatch.setattr(O, "decode_plan", bad)
-    assert _fails(lambda: G.test_plan_covers_each_job_exactly_once(7, 4))
-
-
 def test_prefill_causal_shift(monkeypatch):
     orig = O.prefill_attention
 
