@@ -123,7 +123,11 @@ def test_multi_chunk_prefill(m, n_chunks, kv_dtype):
     def attn_ok(o, l, K, V, cu_k, causal, label):
         ro, rl = O.prefill_attention(q64, f64(K), f64(V), cu_q, cu_k, causal, scale)
         t = prefill_terms(q64, f64(K), f64(V), cu_q, cu_k, causal, scale)
-        check_attention(f64(o), l.cpu().numpy(), ro, rl, t, out_tol=1e-2, lse_tol=1e-3,
+        # the first causal rows see one or two keys, so |o| reaches ~4, where
+        # the bf16 rounding of the output alone (2^-8 relative) exceeds 1e-2:
+        # the max-abs bound gets that documented term
+        check_attention(f64(o), l.cpu().numpy(), ro, rl, t,
+                        out_tol=1e-2 + 2.0 ** -8 * float(np.abs(ro).max()), lse_tol=1e-3,
                         label=label)
 
     def merge_ok(o, l, parts):
