@@ -391,6 +391,73 @@ struct SegWalk {
       return true;
     }
   }
+
+  // next() for a whole warp (every lane gets the same segment): the span's
+  // first job is found by a 32-way search (one round of loads for up to 32
+  // jobs, instead of a chain of dependent loads), and the job's fields and
+  // its request's seq_len are loaded together (s.len is set).
+  __device__ bool next_warp(Seg &s, const int32_t *__restrict__ seq_lens) {
+    const int lane = threadIdx.x & 31;
+    const int total = plan.total(), C = plan.chunk();
+    const int32_t *tp = plan.tile_prefix();
+    while (true) {
+      if (!started) {
+        if (p * C >= total) return false;
+        span_lo = p * C;
+        span_hi = min(total, span_lo + C);
+        // last j in [0, J] with tp[j] <= span_lo (tp[0] = 0, non-decreasing)
+        int a = 0, z = plan.J;
+        while (a < z) {
+          const int stride = (z - a + 32) / 32;         // ceil((z - a + 1) / 32)
+          const int idx = a + lane * stride;
+          const bool le = idx <= z && tp[idx] <= span_lo;
+          const uint32_t mask = __ballot_sync(0xffffffffu, le);
+          const int hi_lane = 31 - __clz(mask);          // lane 0 always qualifies
+          const int na = a + hi_lane * stride;
+          z = min(z, na + stride - 1);
+          a = na;
+          if (stride == 1) break;
+        }
+        j = a;
+        started = true;
+      }
+      if (j >= plan.J) {
+        p += groups;
+        started = false;
+        continue;
+      }
+      const int bi = j / HG, hg = j % HG;
+      const int b = bi / q_len;
+      // independent loads, all in flight together
+      const int t0 = tp[j], t1 = tp[j + 1];
+      const int lo = plan.job_lo()[j], hi = plan.job_hi()[j];
+      const int sp = plan.seg_prefix()[j];
+      const int len = __ldg(seq_lens + b);
+      if (t0 >= span_hi) {
+        p += groups;
+        started = false;
+        continue;
+      }
+      if (t1 <= t0) { ++j; continue; }    // empty job
+      const int a = t0 + kJobCost;        // the job's first tile (after its switch cost)
+      const int u0 = max(span_lo, a), u1 = min(span_hi, t1);
+      if (u1 <= u0) { ++j; continue; }    // the span meets only the switch cost
+      s.job = j;
+      s.b = b;
+      s.row0 = bi * H + hg * 128;
+      s.out_row0 = s.row0;
+      s.hrows = min(128, H - hg * 128);
+      s.lo = lo;
+      s.hi = hi;
+      s.tile0 = lo / tile + (u0 - a);
+      s.ntiles = u1 - u0;
+      s.whole = (span_lo <= a) && (t1 <= span_hi);
+      s.slot = sp + (span_lo / C - a / C);
+      s.len = len;
+      ++j;
+      return true;
+    }
+  }
 };
 
 struct DecodeArgs {
@@ -1064,19 +1131,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       __syncwarp();
       return true;
     };
-    while (ok && walk.next(sg)) {
-      sg.len = __ldg(args.seq_lens + sg.b);
+    while (ok && walk.next_warp(sg, args.seq_lens)) {
       if (!(ok = publish(nseg, false))) break;
-      // The segment's query rows (contiguous, 1152 B each) are read by the
-      // softmax warps when this CTA reaches the segment, about a ring's
-      // worth of tiles from now; a demand load at that point waits behind
-      // every SM's KV stream, so they are pulled into L2 here.
-      if (lane == 0) {
-        const uint8_t *qrows = args.q + static_cast<int64_t>(sg.row0) * kDqk * 2;
-        const uint32_t bytes = static_cast<uint32_t>(sg.hrows) * kDqk * 2;
-        for (uint32_t o = 0; o < bytes; o += 16384)
-          prefetch_l2(qrows + o, min(16384u, bytes - o));
-      }
       const int32_t *bt = args.block_table + static_cast<int64_t>(sg.b) * args.max_blocks;
       int page_base = -(1 << 30), my_blk = -1;
       auto blk_of = [&](int tile) -> int {  // warp-collective
@@ -1120,6 +1176,14 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       const int pre = min(sg.ntiles, 1);
       for (int t = 0; ok && t < pre; ++t) ok = load_tile(sg.tile0 + t);
       if (!ok) break;
+      // The segment's query rows are read by the softmax warps when this CTA
+      // reaches the segment, about a ring's worth of tiles from now; a
+      // demand load at that point waits behind every SM's KV stream, so
+      // this CTA's latent half of each row (512 B) is pulled into L2 here,
+      // after the segment's first tile load (which must not queue behind
+      // it).
+      for (int row = lane; row < sg.hrows; row += 32)
+        prefetch_l2(args.q + (static_cast<int64_t>(sg.row0 + row) * kDqk + 256 * half) * 2, 512);
       if (nseg > 0 && !(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
       if (lane == 0) {
         mbar_arrive_expect_tx(q_full, kQRopeBytes);
