@@ -173,6 +173,73 @@ def v_up(o_lat, w_uv):
 
 
 # --------------------------------------------------------------------------
+# Before the path: rotary position embedding and the cache write
+# --------------------------------------------------------------------------
+
+def rope_inv_freq(dim=R, base=10000.0):
+    """theta_i = base^(-2i/dim) for pair i < dim/2 (the rotary position
+    embedding of RoFormer, Su et al. 2021, §3.2; the pages name the step,
+    rotary_emb, but not its variant: this is the plain reading)."""
+    i = np.arange(dim // 2, dtype=np.float64)
+    return float(base) ** (-2.0 * i / dim)
+
+
+def rope(x, positions, base=10000.0, interleaved=True):
+    """Rotate the last axis of x (even width d) by each token's position.
+
+    MLA DCP query replication digest, §关键源码片段 mla.py: rotary_emb is
+    applied to the rope slice of the query (q[..., qk_nope_head_dim:]) and
+    to k_pe before mla_attn.  Pair i of token t turns by angle
+    positions[t] * theta_i:  (a, b) -> (a cos - b sin, a sin + b cos).
+    interleaved: pair i = dims (2i, 2i+1) (RoFormer's layout);
+    otherwise pair i = dims (i, i + d/2) (the rotate-half layout).
+    x [T, ..., d] (fp64), positions [T] -> same shape."""
+    x = np.asarray(x, dtype=np.float64)
+    d = x.shape[-1]
+    ang = np.asarray(positions, dtype=np.float64)[:, None] * rope_inv_freq(d, base)[None, :]
+    shape = (ang.shape[0],) + (1,) * (x.ndim - 2) + (d // 2,)
+    c, s = np.cos(ang).reshape(shape), np.sin(ang).reshape(shape)
+    if interleaved:
+        a, b = x[..., 0::2], x[..., 1::2]
+    else:
+        a, b = x[..., : d // 2], x[..., d // 2:]
+    ra, rb = a * c - b * s, a * s + b * c
+    out = np.empty_like(x)
+    if interleaved:
+        out[..., 0::2], out[..., 1::2] = ra, rb
+    else:
+        out[..., : d // 2], out[..., d // 2:] = ra, rb
+    return out
+
+
+def cache_write(cache, kv_c_bits, k_pe_bits, slot_mapping, kv_dtype="bf16", k_scale=1.0):
+    """Store new tokens' latent rows kv_c ‖ k_pe into the paged cache.
+
+    MLA DCP prefill blog, §Chunked Prefill 与 LSE Merge (the new tokens'
+    KV is already in the cache when attention runs) and MLA DCP query
+    replication digest, §关键源码片段 mla.py (kv_c_normed and the rotated
+    k_pe are what the attention layer receives).  Token n goes to physical
+    row slot_mapping[n] = block * 64 + offset; a negative slot is padding
+    and writes nothing.  A bf16 cache stores the bits; an e4m3 cache stores
+    e4m3(f32(value) / f32(k_scale)) (round to nearest even, saturating).
+    cache: uint16 bf16 bits or uint8 e4m3 codes [num_blocks, 64, 576];
+    kv_c_bits [T, 512], k_pe_bits [T, 64]: bf16 bits.  Returns a copy."""
+    out = np.array(cache, copy=True)
+    rows = np.concatenate([np.asarray(kv_c_bits, np.uint16),
+                           np.asarray(k_pe_bits, np.uint16)], axis=1)
+    if kv_dtype == "bf16":
+        codes = rows
+    else:
+        vals = codecs.bf16_to_f64(rows).astype(np.float32) / np.float32(k_scale)
+        codes = codecs.f32_to_e4m3(vals)
+    for n, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        if slot < 0:
+            continue
+        out[slot // BLOCK, slot % BLOCK] = codes[n]
+    return out
+
+
+# --------------------------------------------------------------------------
 # A7: paged gather, dequantising gather, interleaved-shard reorg
 # --------------------------------------------------------------------------
 

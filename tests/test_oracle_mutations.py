@@ -8,6 +8,7 @@ import pytest
 import oracle.mla as O
 from tests import test_oracle_decode as D
 from tests import test_oracle_gather_prefill as G
+from tests import test_oracle_rope as RP
 
 
 def _fails(*pins):
@@ -110,3 +111,34 @@ def test_prefill_causal_shift(monkeypatch):
     monkeypatch.setattr(O, "prefill_attention", bad)
     assert _fails(G.test_prefill_causal_brute_force,
                   lambda: G.test_chunked_prefill_equals_full_attention(2))
+
+
+def test_rope_sin_sign_flipped(monkeypatch):
+    """A rotation by -theta keeps norms and relative positions: only the
+    hand-worked example catches it."""
+    orig = O.rope
+    monkeypatch.setattr(O, "rope", lambda x, p, base=10000.0, interleaved=True:
+                        orig(x, -np.asarray(p), base, interleaved))
+    assert _fails(lambda: RP.test_rope_matches_hand_worked_example(True, "interleaved"))
+
+
+def test_rope_frequency_exponent_wrong(monkeypatch):
+    monkeypatch.setattr(O, "rope_inv_freq", lambda dim=64, base=10000.0:
+                        float(base) ** (-np.arange(dim // 2, dtype=np.float64) / dim))
+    assert _fails(lambda: RP.test_rope_matches_hand_worked_example(True, "interleaved"))
+
+
+def test_rope_pairs_wrong(monkeypatch):
+    """Pairs taken as (i, i + d/2) where (2i, 2i + 1) is meant."""
+    orig = O.rope
+    monkeypatch.setattr(O, "rope", lambda x, p, base=10000.0, interleaved=True:
+                        orig(x, p, base, not interleaved))
+    assert _fails(lambda: RP.test_rope_matches_hand_worked_example(True, "interleaved"),
+                  RP.test_rope_layouts_agree_under_the_pairing_permutation)
+
+
+def test_cache_write_skips_no_padding(monkeypatch):
+    orig = O.cache_write
+    monkeypatch.setattr(O, "cache_write", lambda c, kv, kp, slots, dt="bf16", ks=1.0:
+                        orig(c, kv, kp, np.abs(np.asarray(slots)), dt, ks))
+    assert _fails(lambda: RP.test_cache_write_then_gather_returns_the_rows("bf16"))
