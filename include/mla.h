@@ -212,6 +212,36 @@ int mla_decode_plan(const int32_t *seq_lens, const int32_t *kv_starts,
                     mla_stream_t stream);
 
 /* ---------------------------------------------------------------------
+ * Before the path: rotary position embedding and the cache write
+ * [Q-REP] §关键源码片段 mla.py (rotary_emb(positions, q[..., qk_nope_head_dim:],
+ * k_pe) runs before mla_attn); [BLOG] §Chunked Prefill 与 LSE Merge (the
+ * new tokens' KV is already in the cache when attention runs).  The pages
+ * name the rotation but not its variant: this is RoFormer's rotary
+ * embedding (Su et al. 2021), pair i of a 64-wide vector turned by
+ *   theta = positions[t] * rope_base^(-2i/64):
+ *   (a, b) -> (a cos theta - b sin theta, a sin theta + b cos theta),
+ * pairs (2i, 2i+1) for MLA_ROPE_INTERLEAVED, (i, i+32) for MLA_ROPE_HALF.
+ * Angles and their sine / cosine are computed in fp64, the rotation in
+ * fp32, rounded to bf16 once.
+ * For each new token t < T:
+ *   q_pe [T,H,64] bf16 (NULL: no query) is rotated in place;
+ *   k_pe [T,64] bf16 is rotated in place;
+ *   row slot_mapping[t] (= block * 64 + offset) of kv_cache
+ *   [num_blocks,64,576] receives kv_c[t] [512] bf16 ‖ the rotated k_pe[t]:
+ *   the bits for kv_dtype MLA_BF16, e4m3(fp32(x) / k_scale) (RNE,
+ *   saturating) for MLA_E4M3.
+ * A negative slot is padding and writes nothing; a slot >= num_blocks*64
+ * sets MLA_DEVERR_BLOCK_ID and writes nothing.  positions, slot_mapping
+ * [T] int32.  1 < rope_base < inf.  T == 0 is a no-op. */
+enum mla_rope_layout { MLA_ROPE_INTERLEAVED = 0, MLA_ROPE_HALF = 1 };
+
+int mla_rope_cache_write(void *q_pe, void *k_pe, const void *kv_c,
+                         const int32_t *positions, const int32_t *slot_mapping,
+                         int T, int H, float rope_base, int rope_layout,
+                         void *kv_cache, int kv_dtype, float k_scale,
+                         int num_blocks, mla_stream_t stream);
+
+/* ---------------------------------------------------------------------
  * A5/A10  LSE-rescaling merge of partial attention states
  * [BLOG] §Chunked Prefill 与 LSE Merge (merge_attn_states: elementwise
  * O(B*N*V) rescaling) and §DCP 在 Prefill 与 Decode 中的不同角色 (decode

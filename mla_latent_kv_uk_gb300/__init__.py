@@ -22,7 +22,7 @@ __all__ = [
     "mla_version", "mla_status_string", "mla_get_device_error", "mla_selftest_wait_timeout",
     "mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
     "mla_decode_plan", "mla_merge_states", "mla_v_up", "mla_gather_cache",
-    "mla_gather_cache_reorg", "mla_expand_kv", "mla_prefill_attn",
+    "mla_gather_cache_reorg", "mla_expand_kv", "mla_prefill_attn", "mla_rope_cache_write",
 ]
 
 BF16, E4M3, F32 = 0, 1, 2
@@ -50,6 +50,7 @@ _SIGNATURES = {
                                 _p, _p, _i, _p], _i),
     "mla_expand_kv": ([_p, _p, _i, _i, _p, _p, _p], _i),
     "mla_prefill_attn": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p], _i),
+    "mla_rope_cache_write": ([_p, _p, _p, _p, _p, _i, _i, _f, _i, _p, _i, _f, _i, _p], _i),
 }
 
 
@@ -315,3 +316,32 @@ def mla_prefill_attn(q, k, v, cu_q, cu_k, max_q_len, *, causal, sm_scale, out=No
         _ptr(q), _ptr(k), _ptr(v), _ptr(cu_q), _ptr(cu_k), B, Tq, Nk, H, int(max_q_len),
         int(bool(causal)), float(sm_scale), _ptr(out), _ptr(lse), _stream()))
     return out, lse
+
+
+_ROPE_LAYOUT = {"interleaved": 0, "half": 1}
+
+
+def mla_rope_cache_write(q_pe, k_pe, kv_c, positions, slot_mapping, kv_cache, *,
+                         rope_base=10000.0, layout="interleaved", k_scale=1.0):
+    """Rotates q_pe [T,H,64] (or None) and k_pe [T,64] (bf16) in place by
+    positions [T] and stores kv_c [T,512] ‖ k_pe into kv_cache
+    [num_blocks,64,576] (bf16 or e4m3) at slot_mapping [T] (int32)."""
+    _req(k_pe, "k_pe", torch.bfloat16, 2)
+    _req(kv_c, "kv_c", torch.bfloat16, 2)
+    _req(positions, "positions", torch.int32, 1)
+    _req(slot_mapping, "slot_mapping", torch.int32, 1)
+    _req(kv_cache, "kv_cache", (torch.bfloat16, torch.float8_e4m3fn), 3)
+    T = k_pe.shape[0]
+    H = 0
+    if q_pe is not None:
+        _req(q_pe, "q_pe", torch.bfloat16, 3)
+        if q_pe.shape[0] != T or q_pe.shape[2] != 64:
+            raise ValueError("q_pe must be [T, H, 64]")
+        H = q_pe.shape[1]
+    if (k_pe.shape[1] != 64 or tuple(kv_c.shape) != (T, 512) or positions.shape[0] != T
+            or slot_mapping.shape[0] != T or tuple(kv_cache.shape[1:]) != (64, 576)):
+        raise ValueError("rope / cache-write shapes")
+    _check("mla_rope_cache_write", lib.mla_rope_cache_write(
+        _ptr(q_pe), _ptr(k_pe), _ptr(kv_c), _ptr(positions), _ptr(slot_mapping), T, H,
+        float(rope_base), _ROPE_LAYOUT[layout], _ptr(kv_cache), _DTYPE_CODE[kv_cache.dtype],
+        float(k_scale), kv_cache.shape[0], _stream()))

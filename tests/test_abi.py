@@ -34,7 +34,8 @@ def test_header_declares_the_path():
     for want in ["mla_absorb_q", "mla_decode_paged", "mla_decode_plan",
                  "mla_decode_workspace_size", "mla_merge_states", "mla_v_up",
                  "mla_gather_cache", "mla_gather_cache_reorg", "mla_expand_kv",
-                 "mla_prefill_attn", "mla_status_string", "mla_get_device_error"]:
+                 "mla_prefill_attn", "mla_rope_cache_write", "mla_status_string",
+                 "mla_get_device_error"]:
         assert want in names
 
 
@@ -82,6 +83,18 @@ def test_host_validation_rejects_bad_arguments():
     # reorg: W out of range
     assert L.mla_gather_cache_reorg(17, 1, None, None, None, 1, 0, 1.0, None, 1, 0,
                                     0, None, None, None, 0, s) == 1
+    # rope / cache write: bad layout, base <= 1, e4m3 with zero scale, null
+    # pointers; T == 0 is a no-op
+    assert L.mla_rope_cache_write(None, None, None, None, None, 1, 0, 10000.0, 2,
+                                  None, 0, 1.0, 1, s) == 1
+    assert L.mla_rope_cache_write(None, None, None, None, None, 1, 0, 1.0, 0,
+                                  None, 0, 1.0, 1, s) == 1
+    assert L.mla_rope_cache_write(None, None, None, None, None, 1, 0, 10000.0, 0,
+                                  None, 1, 0.0, 1, s) == 1
+    assert L.mla_rope_cache_write(None, None, None, None, None, 1, 0, 10000.0, 0,
+                                  None, 0, 1.0, 1, s) == 1
+    assert L.mla_rope_cache_write(None, None, None, None, None, 0, 0, 10000.0, 0,
+                                  None, 0, 1.0, 1, s) == 0
 
 
 def test_workspace_size_grows_with_work():
