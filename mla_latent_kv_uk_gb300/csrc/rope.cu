@@ -9,13 +9,15 @@
 // RoFormer's rotary embedding (Su et al. 2021): pair i of a 64-wide vector
 // turns by position * base^(-2i/64).
 //
-// One CTA per new token, 128 threads.  The 32 angles of the token are
-// computed in fp64 (one thread per pair, sincos in double) and kept as fp32
-// cos / sin in shared memory; every 16-byte chunk of the query heads, of
-// k_pe and of kv_c is then handled by one thread (loads and stores of 16
-// bytes, the rotation in fp32, one bf16 rounding).  The kernel is a stream
-// of the token's bytes (q_pe in and out, kv_c and k_pe in, one cache row
-// out), bound by memory latency at decode batch sizes.
+// Grid (new tokens, blocks of 32 query heads), 128 threads: each CTA
+// computes its token's 32 angles in fp64 (one thread per pair, sincos in
+// double) and keeps them as fp32 cos / sin in shared memory, then every
+// 16-byte chunk of its 32 query heads is handled by one thread (loads and
+// stores of 16 bytes, the rotation in fp32, one bf16 rounding); the first
+// head block of a token also rotates k_pe and writes the cache row.  The
+// kernel is a stream of the tokens' bytes (q_pe in and out, kv_c and k_pe in,
+// one cache row out), bound by memory latency at decode batch sizes, hence
+// the spread of each token over several CTAs.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <math.h>
@@ -29,6 +31,7 @@ namespace mla {
 namespace {
 
 constexpr int kRopeThreads = 128;
+constexpr int kHeadsPerCta = 32;
 constexpr int kPairs = kRope / 2;   // 32
 
 __device__ __forceinline__ float bf_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -101,7 +104,7 @@ rope_cache_kernel(uint4 *__restrict__ q_pe, uint4 *__restrict__ k_pe,
                   int *err) {
   __shared__ float cs[kPairs], sn[kPairs];
   __shared__ int64_t slot_s;
-  const int t = blockIdx.x, tid = threadIdx.x;
+  const int t = blockIdx.x, hb = blockIdx.y, tid = threadIdx.x;
   if (tid < kPairs) {
     // theta_i = base^(-2i/64); the angle and its sine / cosine in fp64
     const double ang = static_cast<double>(positions[t]) * exp2(-(2.0 * tid / kRope) * log2_base);
@@ -110,7 +113,7 @@ rope_cache_kernel(uint4 *__restrict__ q_pe, uint4 *__restrict__ k_pe,
     cs[tid] = static_cast<float>(c);
     sn[tid] = static_cast<float>(s);
   }
-  if (tid == kPairs) {
+  if (tid == kPairs && hb == 0) {
     int64_t slot = slot_mapping[t];
     if (slot >= num_slots) {
       raise_error(err, MLA_DEVERR_BLOCK_ID);
@@ -119,15 +122,15 @@ rope_cache_kernel(uint4 *__restrict__ q_pe, uint4 *__restrict__ k_pe,
     slot_s = slot;
   }
   __syncthreads();
-  const int64_t slot = slot_s;
-  // query heads: rope rows of 128 B = 8 chunks
+  // this CTA's query heads: rope rows of 128 B = 8 chunks
   if (q_pe) {
-    uint4 *qt = q_pe + static_cast<int64_t>(t) * H * 8;
+    const int h0 = hb * kHeadsPerCta, nh = min(kHeadsPerCta, H - h0);
+    uint4 *qt = q_pe + (static_cast<int64_t>(t) * H + h0) * 8;
     if (!half_layout) {
-      for (int i = tid; i < H * 8; i += kRopeThreads)
+      for (int i = tid; i < nh * 8; i += kRopeThreads)
         qt[i] = rot_interleaved(qt[i], i & 7, cs, sn);
     } else {
-      for (int i = tid; i < H * 4; i += kRopeThreads) {
+      for (int i = tid; i < nh * 4; i += kRopeThreads) {
         uint4 *row = qt + (i >> 2) * 8;
         const int c = i & 3;
         uint4 va = row[c], vb = row[c + 4];
@@ -137,6 +140,8 @@ rope_cache_kernel(uint4 *__restrict__ q_pe, uint4 *__restrict__ k_pe,
       }
     }
   }
+  if (hb != 0) return;   // k_pe and the cache row: the token's first head block
+  const int64_t slot = slot_s;
   uint8_t *dst_row = slot >= 0 ? kv_cache + slot * (fp8 ? kDqk : kDqk * 2) : nullptr;
   // k_pe (in place) and the rope part of the cache row
   uint4 *kt = k_pe + static_cast<int64_t>(t) * 8;
@@ -192,7 +197,8 @@ extern "C" int mla_rope_cache_write(void *q_pe, void *k_pe, const void *kv_c,
     return MLA_ERR_INVALID_ARG;
   int *err = device_error_word();
   if (!err) return MLA_ERR_CUDA;
-  rope_cache_kernel<<<T, kRopeThreads, 0, stream>>>(
+  const dim3 grid(T, q_pe ? (H + kHeadsPerCta - 1) / kHeadsPerCta : 1);
+  rope_cache_kernel<<<grid, kRopeThreads, 0, stream>>>(
       static_cast<uint4 *>(q_pe), static_cast<uint4 *>(k_pe), static_cast<const uint4 *>(kv_c),
       positions, slot_mapping, H, std::log2(static_cast<double>(rope_base)),
       rope_layout == MLA_ROPE_HALF ? 1 : 0, static_cast<uint8_t *>(kv_cache),
