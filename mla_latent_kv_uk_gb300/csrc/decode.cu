@@ -1234,19 +1234,24 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           if (last) mma_commit(q_free);
         }
       };
-      auto issue_qk_chunk = [&](int kcx, int ucx, bool last, int chunk) {
-        static_assert(kQkChunks == 3, "dispatch below covers three chunks");
-        switch (chunk) {
-          case 0: issue_qk_chunk_c(kcx, ucx, last, std::integral_constant<int, 0>{}); break;
-          case 1: issue_qk_chunk_c(kcx, ucx, last, std::integral_constant<int, 1>{}); break;
-          default: issue_qk_chunk_c(kcx, ucx, last, std::integral_constant<int, 2>{}); break;
-        }
+      // All 18 K steps of one tile's QK as one straight-line burst: the
+      // tensor pipe holds only a couple of queued MMAs, so any other work of
+      // this thread between MMAs (a barrier test costs ~70 cycles) idles it.
+      auto issue_qk = [&](int kcx, int ucx, bool last) {
+        issue_qk_chunk_c(kcx, ucx, last, std::integral_constant<int, 0>{});
+        issue_qk_chunk_c(kcx, ucx, last, std::integral_constant<int, 1>{});
+        issue_qk_chunk_c(kcx, ucx, last, std::integral_constant<int, 2>{});
       };
-      // QK of global tile u may start once its KV tile has landed and both
-      // row groups have read the scores of tile u-2 out of the same buffer.
-      auto qk_ready = [&](int kcx, int ucx) -> bool {
-        return mbar_test(&kv_full[kcx % kStages], (kcx / kStages) & 1) &&
-               (ucx < 2 || mbar_test(&s_free[ucx & 1], ((ucx - 2) >> 1) & 1));
+      // QK of global tile u (ring slot kcx) waits until its KV tile has
+      // landed and both row groups have read the scores of tile u-2 out of
+      // the same buffer.
+      auto qk = [&](int kcx, int ucx, bool last) -> bool {
+        if (!mbar_wait(&kv_full[kcx % kStages], (kcx / kStages) & 1, abort_flag)) return false;
+        if (ucx >= 2 && !mbar_wait(&s_free[ucx & 1], ((ucx - 2) >> 1) & 1, abort_flag))
+          return false;
+        tc_fence_after();
+        issue_qk(kcx, ucx, last);
+        return true;
       };
       while (ok) {
         // segment nseg from the producer's queue
@@ -1261,42 +1266,31 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
              mbar_wait(q_tmem, nseg & 1, abort_flag);
         if (!ok) break;
         ++nseg;
-        // QK runs up to two tiles ahead of P.V (bounded by the two score
-        // buffers); P.V of tile t may go out between QK chunks.  `qn`
-        // counts this segment's tiles whose QK has been issued in full.
-        int qn = 0, qchunks = 0;
-        long long t_spin = 0;
-        for (int t = 0; t < sg.ntiles;) {
-          bool progressed = false;
-          if (qn < sg.ntiles && qn < t + 3 &&
-              (qchunks > 0 || qk_ready(kc + (qn - t), uc + (qn - t)))) {
-            if (qchunks == 0) tc_fence_after();
-            issue_qk_chunk(kc + (qn - t), uc + (qn - t), qn + 1 == sg.ntiles, qchunks);
-            if (++qchunks == kQkChunks) { qchunks = 0; ++qn; }
-            progressed = true;
-          }
-          if (qn > t && mbar_test(&p_full[uc & 1], (uc >> 1) & 1)) {
-            tc_fence_after();
-            const uint32_t stage = smem_u32(sm_kv + (kc % kStages) * kStageBytes);
-            const uint32_t pbuf = smem_u32(sm_p + (uc & 1) * kPBuf);
+        // Fixed order, blocking waits: QK of the segment's first two tiles,
+        // then for each tile t the QK of tile t+2 (the scores two tiles
+        // ahead, which the score buffers allow) and the P.V of tile t.  The
+        // scores of tile t are read before its probabilities exist, so
+        // QK(t+2) is ready before P.V(t) and this order never waits on one
+        // while the other could go.
+        const int n = sg.ntiles;
+        for (int u = 0; ok && u < min(2, n); ++u) ok = qk(kc + u, uc + u, u + 1 == n);
+        for (int t = 0; ok && t < n; ++t, ++kc, ++uc) {
+          if (t + 2 < n && !(ok = qk(kc + 2, uc + 2, t + 3 == n))) break;
+          if (!(ok = mbar_wait(&p_full[uc & 1], (uc >> 1) & 1, abort_flag))) break;
+          tc_fence_after();
+          const uint32_t stage = smem_u32(sm_kv + (kc % kStages) * kStageBytes);
+          const uint32_t pbuf = smem_u32(sm_p + (uc & 1) * kPBuf);
 #pragma unroll
-            for (int kk = 0; kk < kPvSteps; ++kk) {
-              // A = P (K-major, 16 tokens per step); B = the four own latent
-              // boxes, MN-major: N-blocks one box apart (LBO), 8-token
-              // groups SBO apart
-              const uint64_t adesc = sdesc(pbuf + kk * 32, 16, 1024, kSwizzle128B);
-              const uint64_t bdesc = sdesc(stage + kk * 2048, kBox, 1024, kSwizzle128B);
-              mma_f16_ss(tmem + kColO, adesc, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-            }
-            mma_commit(&kv_empty[kc % kStages]);
-            mma_commit(&pv_done[uc & 1]);
-            ++t; ++kc; ++uc;
-            progressed = true;
+          for (int kk = 0; kk < kPvSteps; ++kk) {
+            // A = P (K-major, 16 tokens per step); B = the four own latent
+            // boxes, MN-major: N-blocks one box apart (LBO), 8-token
+            // groups SBO apart
+            const uint64_t adesc = sdesc(pbuf + kk * 32, 16, 1024, kSwizzle128B);
+            const uint64_t bdesc = sdesc(stage + kk * 2048, kBox, 1024, kSwizzle128B);
+            mma_f16_ss(tmem + kColO, adesc, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
           }
-          if (progressed) { t_spin = 0; continue; }
-          if (*abort_flag) { ok = false; break; }
-          if (t_spin == 0) t_spin = clock64();
-          else if (clock64() - t_spin > kWaitLimitCycles) { *abort_flag = 1; ok = false; break; }
+          mma_commit(&kv_empty[kc % kStages]);
+          mma_commit(&pv_done[uc & 1]);
         }
       }
       if (!ok) {
