@@ -1170,24 +1170,35 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
         ++kc;
         return true;
       };
-      // The first KV tile of the segment, then its query rope half: the
-      // previous segment's last QK (which frees the rope buffer) completes
-      // about when the stage of this first tile frees up.
+      // The first segment's query rope half goes out before any KV tile
+      // (nothing is in flight yet and QK(0) needs it).  A later segment
+      // loads its first KV tile, then its query rope half: the previous
+      // segment's last QK (which frees the rope buffer) completes about
+      // when the stage of this first tile frees up.
+      const bool first = nseg == 0;
+      if (first && lane == 0) {
+        mbar_arrive_expect_tx(q_full, kQRopeBytes);
+        tma_load_2d(sm_q, &tm_qr, q_full, kLatent + 32 * half, sg.row0);
+      }
       const int pre = min(sg.ntiles, 1);
       for (int t = 0; ok && t < pre; ++t) ok = load_tile(sg.tile0 + t);
       if (!ok) break;
-      // The segment's query rows are read by the softmax warps when this CTA
-      // reaches the segment, about a ring's worth of tiles from now; a
-      // demand load at that point waits behind every SM's KV stream, so
-      // this CTA's latent half of each row (512 B) is pulled into L2 here,
-      // after the segment's first tile load (which must not queue behind
-      // it).
-      for (int row = lane; row < sg.hrows; row += 32)
-        prefetch_l2(args.q + (static_cast<int64_t>(sg.row0 + row) * kDqk + 256 * half) * 2, 512);
-      if (nseg > 0 && !(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(q_full, kQRopeBytes);
-        tma_load_2d(sm_q, &tm_qr, q_full, kLatent + 32 * half, sg.row0);
+      if (!first) {
+        if (!(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
+        if (lane == 0) {
+          mbar_arrive_expect_tx(q_full, kQRopeBytes);
+          tma_load_2d(sm_q, &tm_qr, q_full, kLatent + 32 * half, sg.row0);
+          // The softmax warps read this segment's query rows at the end of
+          // the previous segment, about a ring's worth of tiles from now; a
+          // demand load then waits behind every SM's KV stream, so the
+          // rows (contiguous) are pulled into L2 here, in a few large
+          // prefetches (many small ones would hold up the TMA loads behind
+          // them).
+          const uint8_t *qrows = args.q + static_cast<int64_t>(sg.row0) * kDqk * 2;
+          const uint32_t bytes = static_cast<uint32_t>(sg.hrows) * kDqk * 2;
+          for (uint32_t o = 0; o < bytes; o += 16384)
+            prefetch_l2(qrows + o, min(16384u, bytes - o));
+        }
       }
       ++nseg;
       for (int t = pre; ok && t < sg.ntiles; ++t) ok = load_tile(sg.tile0 + t);
