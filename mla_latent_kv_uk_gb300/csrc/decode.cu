@@ -1016,8 +1016,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                    const __grid_constant__ CUtensorMap tm_kr,
                    const __grid_constant__ CUtensorMap tm_qr,
-                   const __grid_constant__ CUtensorMap tm_out,
-                   const __grid_constant__ CUtensorMap tm_ws, DecodeArgs args) {
+                   DecodeArgs args) {
   using namespace pair;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -1640,122 +1639,66 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       const Seg cur = sg;
       sg = nxt;
       have = have_next;
-      // ---- epilogue: O / l for this CTA's 256 latent columns, all rows.
+      // ---- epilogue: O / l for this CTA's 256 latent columns, all rows,
+      // with plain stores: each 128-byte piece of a row (32 fp32 or 64 bf16
+      // columns) goes through one of two 4 KB staging buffers of this warp
+      // in the idle P tiles and leaves as whole 128-byte rows, four rows per
+      // store instruction.  Nothing waits on the stores; tensor-map stores
+      // from the same buffers would wait for the TMA engine to read each
+      // one, behind the next segment's KV loads (~3.5 us per epilogue).
       const float inv = args.out_scale / (own ? l : l_in);
       const bool row_ok = r < cur.hrows;
       const bool bf16_out = cur.whole && args.out_dtype == MLA_BF16;
-      if (!cur.whole || cur.hrows == 128) {
-        // Every row of this warp's 32-row box belongs to the job (a partial
-        // slot always has 128 rows): tensor-map stores of 128-byte rows
-        // (32 fp32 or 64 bf16 columns) from two 4 KB staging buffers per
-        // warp in the idle P tiles, 128B-swizzled; lane 0 issues them and
-        // the TMA engine drains them while the warp moves on.
-        const CUtensorMap *tm = cur.whole ? &tm_out : &tm_ws;
-        const int y = (cur.whole ? cur.out_row0 : cur.slot * 128) + quarter * 32;
-        uint8_t *stg = sm_p + (warp - 2) * 8192;
+      const int esz = bf16_out ? 2 : 4;
+      // a partial slot always has 128 rows; whole-job rows past the head
+      // count belong to the next query row and are not written
+      const int nrows = cur.whole ? cur.hrows : 128;
+      uint8_t *dst0 = cur.whole
+          ? static_cast<uint8_t *>(args.out) +
+                (static_cast<int64_t>(cur.out_row0) * kLatent + 256 * half) * esz
+          : reinterpret_cast<uint8_t *>(args.ws_o) +
+                (static_cast<int64_t>(cur.slot) * 128 * kLatent + 256 * half) * 4;
+      const int64_t rstride = static_cast<int64_t>(kLatent) * esz;
+      uint4 *stg = reinterpret_cast<uint4 *>(sm_p + (warp - 2) * 8192);
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 64) {
-          // 64 columns per step; the TMEM read goes out before the wait for
-          // the staging buffers, so the two latencies overlap
-          uint32_t o[64];
-          tmem_ld_x64(lane_base + kColO + c, o);
-          auto f = [&](int k) { return __uint_as_float(o[k]) * inv; };
+      for (int c = 0; c < 256; c += 64) {
+        uint32_t o[64];
+        tmem_ld_x64(lane_base + kColO + c, o);
+        auto f = [&](int k) { return __uint_as_float(o[k]) * inv; };
+        // one (bf16) or two (fp32) 128-byte pieces of this row
+#pragma unroll
+        for (int pc = 0; pc < 2; ++pc) {
+          if (bf16_out && pc == 1) break;
+          uint4 *buf = stg + pc * 256;
+          __syncwarp();   // the previous use of `buf` has been read out
           if (bf16_out) {
-            // one 4 KB box per step, the two buffers alternating
-            uint8_t *buf = stg + ((c >> 6) & 1) * 4096;
-            if (c >= 128) {
-              if (lane == 0) bulk_wait_read_1();   // the store two steps back has read `buf`
-              __syncwarp();
-            }
-            uint4 *row = reinterpret_cast<uint4 *>(buf + lane * 128);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-              row[k ^ (lane & 7)] =
+              buf[lane * 8 + (k ^ (lane & 7))] =
                   make_uint4(pack_bf16(f(8 * k), f(8 * k + 1)), pack_bf16(f(8 * k + 2), f(8 * k + 3)),
-                             pack_bf16(f(8 * k + 4), f(8 * k + 5)), pack_bf16(f(8 * k + 6), f(8 * k + 7)));
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) tma_store_2d(tm, buf, 256 * half + c, y);
-          } else {
-            // two 4 KB boxes of 32 fp32 columns per step
-            if (c > 0) {
-              if (lane == 0) bulk_wait_read_all();   // the previous step's stores have read both
-              __syncwarp();
-            }
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              uint4 *row = reinterpret_cast<uint4 *>(stg + hh * 4096 + lane * 128);
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                row[k ^ (lane & 7)] =
-                    make_uint4(__float_as_uint(f(32 * hh + 4 * k)), __float_as_uint(f(32 * hh + 4 * k + 1)),
-                               __float_as_uint(f(32 * hh + 4 * k + 2)),
-                               __float_as_uint(f(32 * hh + 4 * k + 3)));
-            }
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-              tma_store_2d(tm, stg, 256 * half + c, y);
-              tma_store_2d(tm, stg + 4096, 256 * half + c + 32, y);
-            }
-          }
-        }
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
-      } else {
-        // A head group with fewer than 128 rows, written whole: the rows
-        // past it belong to the next query row's heads, so only valid rows
-        // are stored, staged per 32 columns for whole-row-segment stores.
-        uint4 *stage = reinterpret_cast<uint4 *>(sm_p + (warp - 2) * 4096);
-#pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
-          uint32_t o[32];
-          tmem_ld_x32(lane_base + kColO + c, o);
-          float v[32];
-#pragma unroll
-          for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
-          if (bf16_out) {
-            // row = 64 bytes = 4 chunks of 8 bf16
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-              stage[lane * 4 + (k ^ (lane & 3))] =
-                  make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]), pack_bf16(v[8 * k + 2], v[8 * k + 3]),
-                             pack_bf16(v[8 * k + 4], v[8 * k + 5]), pack_bf16(v[8 * k + 6], v[8 * k + 7]));
-          } else {
-            // row = 128 bytes = 8 chunks of 4 fp32
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              stage[lane * 8 + (k ^ (lane & 7))] =
-                  make_uint4(__float_as_uint(v[4 * k]), __float_as_uint(v[4 * k + 1]),
-                             __float_as_uint(v[4 * k + 2]), __float_as_uint(v[4 * k + 3]));
-          }
-          __syncwarp();
-          const int col = 256 * half + c;
-          if (bf16_out) {
-#pragma unroll
-            for (int it = 0; it < 4; ++it) {
-              const int row = it * 8 + (lane >> 2), ch = lane & 3;   // 8 rows per instruction
-              const int R = quarter * 32 + row;
-              if (R < cur.hrows)
-                reinterpret_cast<uint4 *>(static_cast<__nv_bfloat16 *>(args.out) +
-                                          static_cast<int64_t>(cur.out_row0 + R) * kLatent + col)[ch] =
-                    stage[row * 4 + (ch ^ (row & 3))];
-            }
+                             pack_bf16(f(8 * k + 4), f(8 * k + 5)),
+                             pack_bf16(f(8 * k + 6), f(8 * k + 7)));
           } else {
 #pragma unroll
-            for (int it = 0; it < 8; ++it) {
-              const int row = it * 4 + (lane >> 3), ch = lane & 7;   // 4 rows per instruction
-              const int R = quarter * 32 + row;
-              if (R < cur.hrows) {
-                float *base = static_cast<float *>(args.out) +
-                              static_cast<int64_t>(cur.out_row0 + R) * kLatent + col;
-                reinterpret_cast<uint4 *>(base)[ch] = stage[row * 8 + (ch ^ (row & 7))];
-              }
+            for (int k = 0; k < 8; ++k) {
+              const int e = 32 * pc + 4 * k;
+              buf[lane * 8 + (k ^ (lane & 7))] =
+                  make_uint4(__float_as_uint(f(e)), __float_as_uint(f(e + 1)),
+                             __float_as_uint(f(e + 2)), __float_as_uint(f(e + 3)));
             }
           }
           __syncwarp();
+          uint8_t *dst = dst0 + static_cast<int64_t>(c + 32 * pc) * esz;
+#pragma unroll
+          for (int it = 0; it < 8; ++it) {
+            const int row = it * 4 + (lane >> 3), ch = lane & 7;   // 4 rows per instruction
+            const int R = quarter * 32 + row;
+            if (R < nrows)
+              reinterpret_cast<uint4 *>(dst + R * rstride)[ch] = buf[row * 8 + (ch ^ (row & 7))];
+          }
         }
       }
+      __syncwarp();
       // The P tiles are written again in the next segment (own rows, and
       // the peer's rows after our signal), also by other warps of this CTA:
       // every warp's staging has been read out first.
@@ -2053,7 +1996,7 @@ int launch_decode(const void *q, const void *kv_cache, int B, int q_len, int H,
 }
 
 int launch_decode_pair(const void *q, const void *kv_cache, int B, int q_len, int H,
-                       int num_blocks, int64_t ws_slots, DecodeArgs a, mla_stream_t stream) {
+                       int num_blocks, DecodeArgs a, mla_stream_t stream) {
   // KV latent boxes {64 columns, 64 tokens} (128B swizzle); KV and query
   // rope halves {32 columns, 64 tokens / 128 heads} (64B swizzle)
   CUtensorMap tm_kv, tm_kr, tm_qr;
@@ -2071,27 +2014,11 @@ int launch_decode_pair(const void *q, const void *kv_cache, int B, int q_len, in
       !make_tmap(&tm_qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, q_dims, strides, box_qr,
                  CU_TENSOR_MAP_SWIZZLE_64B))
     return MLA_ERR_CUDA;
-  // Epilogue stores: 32-row boxes of 128-byte rows (32 fp32 or 64 bf16),
-  // 128B swizzle, into the output [rows, 512] and the partials [slots*128, 512].
-  CUtensorMap tm_out, tm_ws;
-  const bool out_bf16 = a.out_dtype == MLA_BF16;
-  const uint64_t out_dims[2] = {kLatent, static_cast<uint64_t>(B) * q_len * H};
-  const uint64_t out_strides[1] = {static_cast<uint64_t>(kLatent) * (out_bf16 ? 2 : 4)};
-  const uint32_t box_out[2] = {out_bf16 ? 64u : 32u, 32};
-  const uint64_t ws_dims[2] = {kLatent, static_cast<uint64_t>(ws_slots) * 128};
-  const uint64_t ws_strides[1] = {static_cast<uint64_t>(kLatent) * 4};
-  const uint32_t box_ws[2] = {32, 32};
-  if (!make_tmap(&tm_out,
-                 out_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
-                 a.out, out_dims, out_strides, box_out, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tm_ws, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, a.ws_o, ws_dims, ws_strides, box_ws,
-                 CU_TENSOR_MAP_SWIZZLE_128B))
-    return MLA_ERR_CUDA;
   if (cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            pair::kSmem) != cudaSuccess)
     return MLA_ERR_CUDA;
   PairLaunch pl(a.groups, stream);
-  if (cudaLaunchKernelEx(&pl.cfg, decode_pair_kernel, tm_kv, tm_kr, tm_qr, tm_out, tm_ws, a) !=
+  if (cudaLaunchKernelEx(&pl.cfg, decode_pair_kernel, tm_kv, tm_kr, tm_qr, a) !=
       cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
@@ -2183,8 +2110,7 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   a.ws_lse = ws_lse;
   a.err = err;
   const int st = fp8 ? launch_decode<true>(q, kv_cache, B, q_len, H, num_blocks, a, stream)
-                     : launch_decode_pair(q, kv_cache, B, q_len, H, num_blocks, w.slots, a,
-                                          stream);
+                     : launch_decode_pair(q, kv_cache, B, q_len, H, num_blocks, a, stream);
   if (st != MLA_OK) return st;
 
   const dim3 mgrid(static_cast<unsigned>(J) * (128 / mrg::kRows));
