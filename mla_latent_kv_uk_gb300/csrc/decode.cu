@@ -1405,6 +1405,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     while (ok && have) {
       float m = -INFINITY, l = 0.f;
       const int len = sg.len;
+      int ks = 0;             // forwarding: next message of this segment to send
+      bool staged_s = false;  // ... and whether it is staged in s_send
       for (int t = 0; t < sg.ntiles; ++t, ++uc) {
         const int sb = uc & 1;
         uint8_t *pbuf = sm_p + sb * kPBuf;
@@ -1536,34 +1538,41 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
             if (mbar_wait(&pv_done[sb], (up >> 1) & 1, abort_flag))
               mbar_arrive_remote(peer_smem(&pb_free[sb], peer));
           }
-          // The scores of the next tile of this segment are staged as soon
-          // as QK has produced them and go out as soon as the peer has
-          // consumed the previous message, before or after the
-          // probabilities of this tile come back, whichever is possible
-          // first.  (Not across a segment end: the next segment's QK needs
-          // the query these threads stage after the segment's last tile.)
-          if (t == 0) ok = stage_s(uc) && post_s(uc);
-          if (!ok) break;
+          // Two streams, each served as soon as it can move: the partial
+          // scores of this segment's tiles go out in order, each once QK
+          // has produced it and the peer has consumed the previous message
+          // (however far that runs ahead of this tile), and the
+          // probabilities of this tile come back.  Tying the scores of tile
+          // t+1 to the return of tile t-1 would put two cluster round trips
+          // into every two tiles.  (Not across a segment end: the next
+          // segment's QK needs the query these threads load after the
+          // segment's last tile.)  Messages are staged strictly in order,
+          // so each barrier is tested for the phase right after the last
+          // one this warp has seen complete.
           if (leader) mbar_arrive_expect_tx(&xp_full[sb], kPMsg);
-          bool pending = t + 1 < sg.ntiles, staged = false, got_p = false;
+          bool got_p = false;
           long long t_spin = 0;
-          while (pending || !got_p) {
+          while (!got_p) {
             bool progressed = false;
-            if (pending && !staged) {
-              if (__shfl_sync(0xffffffffu,
-                              mbar_test(&s_full[(uc + 1) & 1], ((uc + 1) >> 1) & 1), 0)) {
-                ok = stage_s(uc + 1);
+            if (ks < sg.ntiles) {
+              const int k = uc - t + ks;   // running tile count of message ks
+              if (!staged_s) {
+                if (__shfl_sync(0xffffffffu, mbar_test(&s_full[k & 1], (k >> 1) & 1), 0)) {
+                  ok = stage_s(k);
+                  if (!ok) break;
+                  staged_s = true;
+                  progressed = true;
+                }
+              } else if (k == 0 ||
+                         __shfl_sync(0xffffffffu, mbar_test(xs_free, (k - 1) & 1), 0)) {
+                ok = post_s(k);
                 if (!ok) break;
-                staged = true;
+                ++ks;
+                staged_s = false;
                 progressed = true;
               }
-            } else if (pending && __shfl_sync(0xffffffffu, mbar_test(xs_free, uc & 1), 0)) {
-              ok = post_s(uc + 1);
-              if (!ok) break;
-              pending = false;
-              progressed = true;
             }
-            if (!got_p && __shfl_sync(0xffffffffu, mbar_test(&xp_full[sb], (uc >> 1) & 1), 0)) {
+            if (__shfl_sync(0xffffffffu, mbar_test(&xp_full[sb], (uc >> 1) & 1), 0)) {
               got_p = true;
               progressed = true;
             }
