@@ -982,6 +982,7 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
 // overlap other tiles' work instead of adding up per tile.
 namespace pair {
 constexpr int kTile = 64;
+constexpr int kThreads = 256;                   // 8 warps, roles below
 constexpr int kStages = 4;
 constexpr int kBox = 8192;                      // 64 tokens x 64 bf16, SW128
 constexpr int kRopeBox = 4096;                  // 64 tokens x 32 bf16, SW64
@@ -1012,7 +1013,7 @@ static_assert(kOffP % 1024 == 0 && kOffQ % 1024 == 0 && kStageBytes % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
 }  // namespace pair
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(pair::kThreads, 1)
 decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                    const __grid_constant__ CUtensorMap tm_kr,
                    const __grid_constant__ CUtensorMap tm_qr,
@@ -1056,6 +1057,19 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
   const int half = static_cast<int>(cluster_rank());
   const uint32_t peer = static_cast<uint32_t>(half ^ 1);
   const int group = blockIdx.x >> 1;
+  // Roles.  A warp reaches only its TMEM lane quadrant (warp % 4), which
+  // holds 32 head rows.  In the two quadrants of this CTA's own rows
+  // ([64*half, 64*half + 64)) warps 4..7 run the online softmax and warps
+  // 0..3 are the TMA producer and the MMA issuer; in the two quadrants of
+  // the forwarded rows warps 0..3 send the partial scores to the peer and
+  // warps 4..7 take the probabilities back (two streams, each served by a
+  // warp of its own, so neither waits behind the other).
+  const int quarter = warp & 3;
+  const bool own = (quarter >> 1) == half;
+  const bool upper = warp >= 4;
+  const bool is_producer = own && !upper && (quarter & 1) == 0;
+  const bool is_mma = own && !upper && (quarter & 1) == 1;
+  const bool is_sender = !own && !upper;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -1064,7 +1078,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
-      mbar_init(&s_free[s], 4);     // lane 0 of each softmax warp
+      mbar_init(&s_free[s], 4);     // lane 0 of each own-row and sending warp
       mbar_init(&p_full[s], 128);
       mbar_init(&pv_done[s], 1);
       mbar_init(&xp_full[s], 1);
@@ -1078,9 +1092,9 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     mbar_init(xs_free, 2);          // lane 0 of each of the peer's own-row warps
     for (int s = 0; s < kSegSlots; ++s) {
       mbar_init(&seg_full[s], 1);
-      mbar_init(&seg_empty[s], 5);  // the MMA thread and lane 0 of each softmax warp
+      mbar_init(&seg_empty[s], 7);  // the MMA thread and lane 0 of six warps
     }
-    mbar_init(stage_ok, 4);         // lane 0 of each softmax warp, once per segment
+    mbar_init(stage_ok, 4);         // lane 0 of warps 4..7, once per segment
     mbar_init(epi_done, 4);         // likewise
     *abort_flag = 0;
     fence_barrier_init();
@@ -1103,7 +1117,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
   walk.init(args.plan, args.J, args.q_len, args.H, args.HG, args.groups, group, kTile);
   Seg sg;
 
-  if (warp == 0) {
+  if (is_producer) {
     // -------------------------------------------------- TMA producer
     if (lane == 0) {
       prefetch_tmap(&tm_kv);
@@ -1209,7 +1223,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
         mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &no_abort);
       if (nseg > 0) mbar_wait(q_full, (nseg - 1) & 1, &no_abort);
     }
-  } else if (warp == 1) {
+  } else if (is_mma) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
       const uint32_t idesc_qk = idesc_bf16(128, kTile, false, false);
@@ -1309,18 +1323,69 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
         mbar_wait(drain, 0, &no_abort);
       }
     }
+  } else if (is_sender) {
+    // ------------------------------- forwarded rows: partial scores out
+    // Every tile's partial scores of this warp's 32 rows, in order, each as
+    // soon as QK has produced it and the peer has consumed the previous
+    // message: TMEM -> s_send (128B-swizzled rows) -> one 8 KB bulk copy
+    // into the same place of the peer's s_recv.  The staging buffer is free
+    // once this warp's previous copy has been read out of it.
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
+    const int lr = r & 63;
+    const int wl = lr >> 5;
+    const uint32_t peer_s_recv = peer_smem(s_recv, peer);
+    const uint32_t peer_xs_full = peer_smem(xs_full, peer);
+    auto warp_ok = [](bool v) { return __all_sync(0xffffffffu, v); };
+    int ns = 0, k = 0;
+    bool ok = true;
+    while (ok) {
+      const int slot = ns % kSegSlots;
+      if (!warp_ok(mbar_wait(&seg_full[slot], (ns / kSegSlots) & 1, abort_flag))) break;
+      const int ntiles = segq[slot].ntiles;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&seg_empty[slot]);
+      ++ns;
+      if (ntiles < 0) break;
+      for (int t = 0; t < ntiles; ++t, ++k) {
+        if (!warp_ok(mbar_wait(&s_full[k & 1], (k >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sv[kTile];
+        tmem_ld_x32(lane_base + kColS + kTile * (k & 1), sv);
+        tmem_ld_x32(lane_base + kColS + kTile * (k & 1) + 32, sv + 32);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&s_free[k & 1]);   // this warp's score rows are read
+          bulk_wait_read_all();          // its copy of tile k-1 has left s_send
+        }
+        __syncwarp();
+        uint4 *dst = reinterpret_cast<uint4 *>(s_send + lr * 256);
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+          dst[j ^ (lr & 15)] = make_uint4(sv[4 * j], sv[4 * j + 1], sv[4 * j + 2], sv[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (k > 0 && !warp_ok(mbar_wait(xs_free, (k - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        if (lane == 0)
+          bulk_copy_to_peer(peer_s_recv + wl * (kSMsg / 2), s_send + wl * (kSMsg / 2),
+                            kSMsg / 2, peer_xs_full);
+      }
+    }
   } else {
-    // ------------------------- softmax (own rows) / forwarding (peer rows)
-    const int quarter = warp & 3;
+    // ------------------- softmax (own rows) / probabilities in (forwarded)
     const int r = quarter * 32 + lane;        // head row within the group
     const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
-    const int tid = threadIdx.x - 64;         // 0..127
-    const bool own = (r >> 6) == half;
+    const int tid = threadIdx.x - 128;        // 0..127
     const int lr = r & 63;                    // row within a message
     const bool leader = lr == 0;              // one thread per 64-thread group
     const int wl = lr >> 5;                   // warp within the group
-    const uint32_t peer_s_recv = peer_smem(s_recv, peer);
-    const uint32_t peer_xs_full = peer_smem(xs_full, peer);
     const uint32_t peer_xs_free = peer_smem(xs_free, peer);
     int uc = 0;
     bool ok = true;
@@ -1347,41 +1412,6 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       tc_fence_before();
       mbar_arrive(q_tmem);
     };
-    // Forwarded rows: partial scores of tile k (global count) -> s_send.
-    // The staging buffer is free as soon as this warp's copy of tile k-1 has
-    // been read out of it, which is usually long before the peer has
-    // consumed that message, so staging runs ahead of the peer.
-    auto stage_s = [&](int k) -> bool {
-      if (!warp_ok(mbar_wait(&s_full[k & 1], (k >> 1) & 1, abort_flag))) return false;
-      tc_fence_after();
-      uint32_t sv[kTile];
-      tmem_ld_x32(lane_base + kColS + kTile * (k & 1), sv);
-      tmem_ld_x32(lane_base + kColS + kTile * (k & 1) + 32, sv + 32);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&s_free[k & 1]);   // this warp's score rows are read
-        bulk_wait_read_all();          // its copy of tile k-1 has left s_send
-      }
-      __syncwarp();
-      uint4 *dst = reinterpret_cast<uint4 *>(s_send + lr * 256);
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        dst[j ^ (lr & 15)] = make_uint4(sv[4 * j], sv[4 * j + 1], sv[4 * j + 2], sv[4 * j + 3]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      return true;
-    };
-    // Staged scores of tile k -> the peer, once it has consumed message k-1
-    // (its s_recv is free): this warp's 32 rows, 8 KB contiguous, to the
-    // same place in the peer.
-    auto post_s = [&](int k) -> bool {
-      if (k > 0 && !warp_ok(mbar_wait(xs_free, (k - 1) & 1, abort_flag))) return false;
-      if (lane == 0)
-        bulk_copy_to_peer(peer_s_recv + wl * (kSMsg / 2), s_send + wl * (kSMsg / 2), kSMsg / 2,
-                          peer_xs_full);
-      return true;
-    };
     // Takes the next segment descriptor from the producer's queue
     // (warp-wide); false at the end marker or on a timeout (then ok = false).
     int ns = 0;
@@ -1405,8 +1435,6 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     while (ok && have) {
       float m = -INFINITY, l = 0.f;
       const int len = sg.len;
-      int ks = 0;             // forwarding: next message of this segment to send
-      bool staged_s = false;  // ... and whether it is staged in s_send
       for (int t = 0; t < sg.ntiles; ++t, ++uc) {
         const int sb = uc & 1;
         uint8_t *pbuf = sm_p + sb * kPBuf;
@@ -1530,7 +1558,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
             bulk_copy_to_peer(peer_smem(al_dst, peer), al, kAlMsg / 2, xbar);
           }
         } else {
-          // ------------------------------------------------ forwarding
+          // ------------------------------------- forwarded rows: P back
           // Our P.V of tile uc-2 is done: the peer may overwrite our P tile
           // `sb` with its rows of tile uc.
           if (leader && uc >= 2) {
@@ -1538,50 +1566,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
             if (mbar_wait(&pv_done[sb], (up >> 1) & 1, abort_flag))
               mbar_arrive_remote(peer_smem(&pb_free[sb], peer));
           }
-          // Two streams, each served as soon as it can move: the partial
-          // scores of this segment's tiles go out in order, each once QK
-          // has produced it and the peer has consumed the previous message
-          // (however far that runs ahead of this tile), and the
-          // probabilities of this tile come back.  Tying the scores of tile
-          // t+1 to the return of tile t-1 would put two cluster round trips
-          // into every two tiles.  (Not across a segment end: the next
-          // segment's QK needs the query these threads load after the
-          // segment's last tile.)  Messages are staged strictly in order,
-          // so each barrier is tested for the phase right after the last
-          // one this warp has seen complete.
           if (leader) mbar_arrive_expect_tx(&xp_full[sb], kPMsg);
-          bool got_p = false;
-          long long t_spin = 0;
-          while (!got_p) {
-            bool progressed = false;
-            if (ks < sg.ntiles) {
-              const int k = uc - t + ks;   // running tile count of message ks
-              if (!staged_s) {
-                if (__shfl_sync(0xffffffffu, mbar_test(&s_full[k & 1], (k >> 1) & 1), 0)) {
-                  ok = stage_s(k);
-                  if (!ok) break;
-                  staged_s = true;
-                  progressed = true;
-                }
-              } else if (k == 0 ||
-                         __shfl_sync(0xffffffffu, mbar_test(xs_free, (k - 1) & 1), 0)) {
-                ok = post_s(k);
-                if (!ok) break;
-                ++ks;
-                staged_s = false;
-                progressed = true;
-              }
-            }
-            if (__shfl_sync(0xffffffffu, mbar_test(&xp_full[sb], (uc >> 1) & 1), 0)) {
-              got_p = true;
-              progressed = true;
-            }
-            if (progressed) continue;
-            if (*abort_flag) { ok = false; break; }
-            if (t_spin == 0) t_spin = clock64();
-            else if (clock64() - t_spin > kWaitLimitCycles) { *abort_flag = 1; ok = false; break; }
-          }
-          ok = warp_ok(ok && mbar_wait(&xp_full[sb], (uc >> 1) & 1, abort_flag));
+          ok = warp_ok(mbar_wait(&xp_full[sb], (uc >> 1) & 1, abort_flag));
           if (!ok) break;
           // the peer's P rows are already in our P tile; apply its factors
           const float *al =
@@ -1668,7 +1654,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           : reinterpret_cast<uint8_t *>(args.ws_o) +
                 (static_cast<int64_t>(cur.slot) * 128 * kLatent + 256 * half) * 4;
       const int64_t rstride = static_cast<int64_t>(kLatent) * esz;
-      uint4 *stg = reinterpret_cast<uint4 *>(sm_p + (warp - 2) * 8192);
+      uint4 *stg = reinterpret_cast<uint4 *>(sm_p + (warp - 4) * 8192);
 #pragma unroll 1
       for (int c = 0; c < 256; c += 64) {
         uint32_t o[64];
@@ -1886,7 +1872,7 @@ struct PairLaunch {
   cudaLaunchAttribute attr[2];
   PairLaunch(int clusters, cudaStream_t stream) {
     cfg.gridDim = dim3(2 * clusters);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(pair::kThreads);
     cfg.dynamicSmemBytes = pair::kSmem;
     cfg.stream = stream;
     attr[0].id = cudaLaunchAttributeClusterDimension;
