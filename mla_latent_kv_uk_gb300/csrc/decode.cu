@@ -925,9 +925,13 @@ decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
 #pragma unroll
         for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
         const int col = 256 * half + c;
-        if (cur.whole && args.out_dtype == MLA_BF16) {
-          uint4 *dst = reinterpret_cast<uint4 *>(
-              static_cast<__nv_bfloat16 *>(args.out) + orow * kLatent + col);
+        if (args.out_dtype == MLA_BF16) {
+          // partials take the output's type
+          __nv_bfloat16 *base =
+              cur.whole ? static_cast<__nv_bfloat16 *>(args.out) + orow * kLatent + col
+                        : reinterpret_cast<__nv_bfloat16 *>(args.ws_o) +
+                              (static_cast<int64_t>(cur.slot) * 128 + r) * kLatent + col;
+          uint4 *dst = reinterpret_cast<uint4 *>(base);
 #pragma unroll
           for (int k = 0; k < 4; ++k)
             dst[k] = make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]),
@@ -1643,7 +1647,9 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       // one, behind the next segment's KV loads (~3.5 us per epilogue).
       const float inv = args.out_scale / (own ? l : l_in);
       const bool row_ok = r < cur.hrows;
-      const bool bf16_out = cur.whole && args.out_dtype == MLA_BF16;
+      // partials take the output's type (a bf16 output is rounded to bf16
+      // anyway; the merge adds at most half a bf16 step of each part)
+      const bool bf16_out = args.out_dtype == MLA_BF16;
       const int esz = bf16_out ? 2 : 4;
       // a partial slot always has 128 rows; whole-job rows past the head
       // count belong to the next query row and are not written
@@ -1652,7 +1658,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           ? static_cast<uint8_t *>(args.out) +
                 (static_cast<int64_t>(cur.out_row0) * kLatent + 256 * half) * esz
           : reinterpret_cast<uint8_t *>(args.ws_o) +
-                (static_cast<int64_t>(cur.slot) * 128 * kLatent + 256 * half) * 4;
+                (static_cast<int64_t>(cur.slot) * 128 * kLatent + 256 * half) * esz;
       const int64_t rstride = static_cast<int64_t>(kLatent) * esz;
       uint4 *stg = reinterpret_cast<uint4 *>(sm_p + (warp - 4) * 8192);
 #pragma unroll 1
@@ -1730,25 +1736,34 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
 // any number of parts works.
 namespace mrg {
 constexpr int kRows = 16;
-constexpr int kRing = 3;
-constexpr int kPartFloats = kRows * kLatent;
-constexpr int kPartBytes = kPartFloats * 4;      // 32 KB
+constexpr int kRingBytes = 96 * 1024;
 constexpr int kLseBytes = kRows * 4;
-constexpr int kOffLse = kRing * kPartBytes;
-constexpr int kOffBars = kOffLse + kRing * kLseBytes;
-constexpr int kSmem = kOffBars + kRing * 8 + 16 + 128;
+// Parts are stored in the output's type (T): 16 rows x 512 of them per
+// part, a ring of as many as fit in kRingBytes (3 fp32 or 6 bf16 parts).
+template <typename T>
+struct Geo {
+  static constexpr int kPartElems = kRows * kLatent;
+  static constexpr int kPartBytes = kPartElems * static_cast<int>(sizeof(T));
+  static constexpr int kRing = kRingBytes / kPartBytes;
+  static constexpr int kOffLse = kRing * kPartBytes;
+  static constexpr int kOffBars = kOffLse + kRing * kLseBytes;
+  static constexpr int kSmem = kOffBars + kRing * 8 + 16 + 128;
+};
 }  // namespace mrg
 
 template <typename Tout>
 __global__ void __launch_bounds__(256, 2)
 decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
-                    const float *__restrict__ ws_o,
+                    const Tout *__restrict__ ws_o,
                     const float *__restrict__ ws_lse, Tout *out, float *lse, int *err) {
   using namespace mrg;
+  using G = mrg::Geo<Tout>;
+  constexpr int kRing = G::kRing, kPartBytes = G::kPartBytes, kPartElems = G::kPartElems;
+  constexpr int kOffLse = G::kOffLse, kOffBars = G::kOffBars;
   extern __shared__ __align__(128) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
-  float *parts = reinterpret_cast<float *>(smem);
+  Tout *parts = reinterpret_cast<Tout *>(smem);
   const float *lses = reinterpret_cast<const float *>(smem + kOffLse);
   uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBars);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(full + kRing);
@@ -1779,7 +1794,7 @@ decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
       const int b = s % kRing;
       const int64_t slot = s0 + s;
       mbar_arrive_expect_tx(&full[b], kPartBytes + kLseBytes);
-      bulk_load(parts + b * kPartFloats, ws_o + (slot * 128 + rb * kRows) * kLatent, kPartBytes,
+      bulk_load(parts + b * kPartElems, ws_o + (slot * 128 + rb * kRows) * kLatent, kPartBytes,
                 &full[b]);
       bulk_load(smem + kOffLse + b * kLseBytes, ws_lse + slot * 128 + rb * kRows, kLseBytes,
                 &full[b]);
@@ -1798,10 +1813,17 @@ decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
         const float sc = expf(m - mn), w = expf(ls - mn);
         z = z * sc + w;
         m = mn;
-        const float4 *src = reinterpret_cast<const float4 *>(parts + b * kPartFloats + lr * kLatent);
+        const Tout *row = parts + b * kPartElems + lr * kLatent;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
-          const float4 v = src[q0 + 16 * k];
+          float4 v;
+          if constexpr (std::is_same<Tout, float>::value) {
+            v = reinterpret_cast<const float4 *>(row)[q0 + 16 * k];
+          } else {
+            const uint2 w = reinterpret_cast<const uint2 *>(row)[q0 + 16 * k];
+            v = make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xFFFF0000u),
+                            __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xFFFF0000u));
+          }
           acc[4 * k] = fmaf(w, v.x, acc[4 * k] * sc);
           acc[4 * k + 1] = fmaf(w, v.y, acc[4 * k + 1] * sc);
           acc[4 * k + 2] = fmaf(w, v.z, acc[4 * k + 2] * sc);
@@ -2110,21 +2132,25 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
 
   const dim3 mgrid(static_cast<unsigned>(J) * (128 / mrg::kRows));
   const int32_t *cplan = plan;
-  const float *cws_o = ws_o, *cws_lse = ws_lse;
+  const float *cws_lse = ws_lse;
   cudaError_t e;
   if (out_dtype == MLA_BF16) {
+    // the partials were written in bf16
+    constexpr int smem = mrg::Geo<__nv_bfloat16>::kSmem;
     e = cudaFuncSetAttribute(decode_merge_kernel<__nv_bfloat16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, mrg::kSmem);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
-      e = launch_pdl(decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(256), mrg::kSmem, stream,
-                     cplan, J, H, HG, cws_o, cws_lse, static_cast<__nv_bfloat16 *>(out), lse,
-                     err);
+      e = launch_pdl(decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(256), smem, stream, cplan, J,
+                     H, HG, reinterpret_cast<const __nv_bfloat16 *>(ws_o), cws_lse,
+                     static_cast<__nv_bfloat16 *>(out), lse, err);
   } else {
+    constexpr int smem = mrg::Geo<float>::kSmem;
     e = cudaFuncSetAttribute(decode_merge_kernel<float>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, mrg::kSmem);
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
-      e = launch_pdl(decode_merge_kernel<float>, mgrid, dim3(256), mrg::kSmem, stream, cplan, J,
-                     H, HG, cws_o, cws_lse, static_cast<float *>(out), lse, err);
+      e = launch_pdl(decode_merge_kernel<float>, mgrid, dim3(256), smem, stream, cplan, J, H, HG,
+                     static_cast<const float *>(ws_o), cws_lse, static_cast<float *>(out), lse,
+                     err);
   }
   return e == cudaSuccess ? MLA_OK : MLA_ERR_CUDA;
 }

@@ -3,8 +3,9 @@ CPU: they must admit a result computed with exactly the roundings the
 decode kernel performs (fp32 scores, bf16 P with an unrounded normaliser,
 bf16 output), and must reject a plausible kernel mistake that the
 spec max-abs tolerance (1e-2) lets through at the tiny config's
-magnitudes.  The mistakes are planted in a CPU emulation built on the
-oracle's own definitions; no GPU result is involved."""
+magnitudes.  The split path (bf16 partials of a job cut into spans, merged
+in fp32) is emulated as well.  The mistakes are planted in a CPU emulation
+built on the oracle's own definitions; no GPU result is involved."""
 
 import math
 
@@ -55,6 +56,46 @@ def _emulate_decode(q, cache, block_table, seq_lens, sm_scale, *, drop_last_tile
     return out, lse
 
 
+def _emulate_split_decode(q, cache, block_table, seq_lens, sm_scale, seg=64):
+    """The split path: each request's key range cut into `seg`-token parts,
+    each part computed as above and stored as a bf16 partial (O / l rounded
+    to bf16, its lse in fp32), then the merge kernel's fp32 online fold
+    (running max, rescaled sum and accumulator, parts in order) and one
+    bf16 rounding of acc * (1 / z)."""
+    B, q_len, H, _ = q.shape
+    out = np.zeros((B, q_len, H, 512))
+    lse = np.full((B, q_len, H), -np.inf)
+    c = np.float32(sm_scale * LOG2E)
+    ln2 = np.float32(math.log(2.0))
+    for b in range(B):
+        for i in range(q_len):
+            lo, hi = O.decode_range(int(seq_lens[b]), q_len, i, True)
+            if hi <= lo:
+                continue
+            m = np.full((H,), -np.inf, np.float32)
+            z = np.zeros((H,), np.float32)
+            acc = np.zeros((H, 512), np.float32)
+            for a in range(lo, hi, seg):
+                blk, off = O.page_rows(block_table[b], np.arange(a, min(hi, a + seg)))
+                rows = cache[blk, off].astype(np.float32)
+                x = ((q[b, i].astype(np.float32) @ rows.T) * c).astype(np.float32)
+                ms = x.max(axis=1, keepdims=True)
+                p = np.exp2(x - ms).astype(np.float32)
+                ls = p.sum(axis=1, keepdims=True, dtype=np.float32)
+                part = _bf16((_bf16(p).astype(np.float32) @ rows[:, :512]).astype(np.float32)
+                             / ls).astype(np.float32)
+                lse_s = ((ms[:, 0] + np.log2(ls[:, 0])) * ln2).astype(np.float32)
+                mn = np.maximum(m, lse_s)
+                sc = np.exp(m - mn).astype(np.float32)
+                w = np.exp(lse_s - mn).astype(np.float32)
+                z = (z * sc + w).astype(np.float32)
+                acc = (acc * sc[:, None] + w[:, None] * part).astype(np.float32)
+                m = mn
+            out[b, i] = _bf16(acc * (np.float32(1.0) / z)[:, None])
+            lse[b, i] = (m + np.log(z)).astype(np.float32)
+    return out, lse
+
+
 @pytest.fixture(scope="module")
 def tiny():
     case = synth.config1(poison=False)
@@ -67,6 +108,17 @@ def tiny():
 def test_bounds_admit_the_kernel_roundings(tiny):
     case, q, cache, ref_o, ref_l, t = tiny
     o, l = _emulate_decode(q, cache, case.block_table, case.seq_lens, case.sm_scale)
+    d_o, r_o, d_l, r_l, finite = bound_report(o, l, ref_o, ref_l, t)
+    assert finite and r_o <= 0.6 and r_l <= 0.6, (r_o, r_l)
+
+
+@pytest.mark.parametrize("seg", [64, 128])
+def test_bounds_admit_the_split_path_with_bf16_partials(tiny, seg):
+    """A job cut into spans stores each span's O / l in the output's type
+    (bf16 here) and merges the parts in fp32: the rounding of the parts
+    stays inside the same bounds."""
+    case, q, cache, ref_o, ref_l, t = tiny
+    o, l = _emulate_split_decode(q, cache, case.block_table, case.seq_lens, case.sm_scale, seg)
     d_o, r_o, d_l, r_l, finite = bound_report(o, l, ref_o, ref_l, t)
     assert finite and r_o <= 0.6 and r_l <= 0.6, (r_o, r_l)
 
