@@ -16,22 +16,26 @@
 //  * The fp32 output of 128 heads x 512 latent columns is exactly one SM's
 //    TMEM, so each work span is processed by a PAIR of CTAs, CTA c owning
 //    latent output columns [256c, 256c + 256).
-//  * bf16 (decode_pair_kernel): the pair is a 2-CTA cluster that splits the
-//    QK contraction by columns.  Each CTA loads only its latent half and its
-//    half of the rope columns of every KV tile, and the partial scores are
-//    summed through distributed shared memory (see the kernel's comment).
-//  * e4m3 (decode_kernel<true>): each CTA of the pair loads whole 36 KB
-//    tiles and recomputes S itself (the second read of a tile is an L2 hit).
-//  * Warp roles: warp 0 TMA producer, warp 1 MMA issuer (+ TMEM owner), the
-//    other warps online softmax (one head row per thread), correction and
-//    epilogue.  Lazy rescaling: O is rescaled only when a row max grows by
-//    more than 2^8.
+//  * decode_pair_kernel<FP8> (bf16 or e4m3 cache): the pair is a 2-CTA
+//    cluster that splits the QK contraction by columns.  Each CTA loads
+//    only its latent half and its half of the rope columns of every KV
+//    tile, and the partial scores are summed through distributed shared
+//    memory (see the kernel's comment).  The e4m3 format uses the same
+//    layout with half-size stages (twice as many in the ring), kind::f8f6f4
+//    MMAs and e4m3 probabilities.
+//  * Warp roles (8 warps, by the CTA's rank): TMA producer, MMA issuer,
+//    online softmax of the CTA's own head rows (one row per thread), the
+//    sending of the forwarded rows' partial scores, and the return of their
+//    probabilities; the softmax and return warps also write the epilogue.
+//    Lazy rescaling: O is rescaled only when a row max grows by more than
+//    2^8.
 //  * Work split (A3): every job (request, query token, 128-head group)
 //    contributes the 64-token tiles its key range touches, preceded by
 //    kJobCost units that stand for the cost of switching to it; jobs are
 //    laid end to end and CTA pair p takes units [p*C, (p+1)*C).  A job cut
-//    into several spans writes fp32 partials that a merge kernel combines
-//    (one CTA per 16 rows, partials streamed in by bulk copies).
+//    into several spans writes partials (in the output's type) that a merge
+//    kernel combines (one CTA per 16 rows, partials streamed in by bulk
+//    copies).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <math.h>
@@ -49,7 +53,6 @@ namespace {
 
 using namespace sm100;
 
-constexpr int kThreads = 192;
 constexpr int kMinTiles = 4;                 // smallest auto span
 // Units of the flat split space a non-empty job takes on top of its tiles:
 // switching a CTA pair to a job costs its epilogue and query load, measured
@@ -59,38 +62,6 @@ constexpr int kMinTiles = 4;                 // smallest auto span
 constexpr int kJobCost = 4;
 constexpr float kRescaleLog2 = 8.f;          // lazy rescale threshold
 constexpr uint32_t kColO = 0, kColS = 256;   // TMEM columns (both variants)
-
-// Tile geometry of the two KV formats.  Boxes are TMA boxes of 64 latent
-// columns; a KV tile holds 9 of them (576 columns).
-template <bool FP8>
-struct Geo;
-
-template <>
-struct Geo<false> {                          // bf16: only the tile width (the
-  static constexpr int kTile = 64;           // kernel geometry is `pair` below)
-};
-
-template <>
-struct Geo<true> {                           // e4m3 cache and query
-  static constexpr int kTile = 64;
-  static constexpr int kStages = 4;
-  static constexpr int kRowBytes = 64;       // 64 e4m3 per box row
-  static constexpr int kBox = kTile * kRowBytes;          // 4 KB
-  static constexpr int kStageBytes = 9 * kBox;            // 36 KB
-  static constexpr int kQBox = 128 * kRowBytes;           // 8 KB
-  static constexpr int kQsBoxes = 9;         // the whole query in smem
-  static constexpr int kQtCols = 0;
-  static constexpr uint32_t kColQ = 0;
-  static constexpr int kKStep = 32;
-  static constexpr uint32_t kSwizzle = sm100::kSwizzle64B;
-  static constexpr uint32_t kSBO = 512;      // 8 rows x 64 B
-};
-
-template <bool FP8>
-constexpr int smem_bytes() {
-  return Geo<FP8>::kQsBoxes * Geo<FP8>::kQBox +
-         Geo<FP8>::kStages * Geo<FP8>::kStageBytes + 256 + 1024;
-}
 
 // ----------------------------------------------------------------- planner
 // Plan layout (int32): [0] total units, [1] C, [2] J, [3] spans, then
@@ -347,52 +318,7 @@ struct SegWalk {
     started = false;
   }
 
-  // Advances to the next segment of this CTA pair; false when done.
-  __device__ bool next(Seg &s) {
-    const int total = plan.total(), C = plan.chunk();
-    const int32_t *tp = plan.tile_prefix();
-    while (true) {
-      if (!started) {
-        if (p * C >= total) return false;
-        span_lo = p * C;
-        span_hi = min(total, span_lo + C);
-        // first job whose tiles contain span_lo
-        int a = 0, z = plan.J;  // last j with tp[j] <= span_lo
-        while (a < z) {
-          int mid = (a + z + 1) >> 1;
-          if (tp[mid] <= span_lo) a = mid; else z = mid - 1;
-        }
-        j = a;
-        started = true;
-      }
-      if (j >= plan.J || tp[j] >= span_hi) {
-        p += groups;
-        started = false;
-        continue;
-      }
-      const int z = tp[j + 1];
-      if (z <= tp[j]) { ++j; continue; }  // empty job
-      const int a = tp[j] + kJobCost;     // the job's first tile (after its switch cost)
-      const int u0 = max(span_lo, a), u1 = min(span_hi, z);
-      if (u1 <= u0) { ++j; continue; }    // the span meets only the switch cost
-      s.job = j;
-      const int bi = j / HG, hg = j % HG;
-      s.b = bi / q_len;
-      s.row0 = bi * H + hg * 128;
-      s.out_row0 = s.row0;
-      s.hrows = min(128, H - hg * 128);
-      s.lo = plan.job_lo()[j];
-      s.hi = plan.job_hi()[j];
-      s.tile0 = s.lo / tile + (u0 - a);
-      s.ntiles = u1 - u0;
-      s.whole = (span_lo <= a) && (z <= span_hi);
-      s.slot = plan.seg_prefix()[j] + (span_lo / C - a / C);
-      ++j;
-      return true;
-    }
-  }
-
-  // next() for a whole warp (every lane gets the same segment): the span's
+  // The next segment of this CTA pair, for a whole warp (every lane gets it): the span's
   // first job is found by a 32-way search (one round of loads for up to 32
   // jobs, instead of a chain of dependent loads), and the job's fields and
   // its request's seq_len are loaded together (s.len is set).
@@ -492,482 +418,10 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c,
   return static_cast<uint32_t>(lo) | (static_cast<uint32_t>(hi) << 16);
 }
 
-template <bool FP8>
-__global__ void __launch_bounds__(kThreads, 1)
-decode_kernel(const __grid_constant__ CUtensorMap tm_kv,
-              const __grid_constant__ CUtensorMap tm_q, DecodeArgs args) {
-  using G = Geo<FP8>;
-  constexpr int kTile = G::kTile;
-  constexpr int kStages = G::kStages;
-  constexpr int kBox = G::kBox;
-  constexpr int kStageBytes = G::kStageBytes;
-  constexpr int kQBox = G::kQBox;
-  constexpr int kQsBoxes = G::kQsBoxes;
-  constexpr int kQsFirstCol = 576 - 64 * kQsBoxes;   // first query column in smem
-  constexpr int kQkSteps = 576 / G::kKStep;           // 36 (bf16) / 18 (e4m3)
-  constexpr int kStepsPerBox = 64 / G::kKStep;        // 4 / 2
-  constexpr int kTmemQSteps = G::kQtCols * 2 / G::kKStep;  // 24 / 0
-  constexpr int kPvSteps = kTile / G::kKStep;         // 2 / 2
-
-  extern __shared__ __align__(1024) uint8_t smem_raw[];
-  uint8_t *smem = reinterpret_cast<uint8_t *>(
-      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sm_q = smem;
-  uint8_t *sm_kv = smem + kQsBoxes * kQBox;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_kv + kStages * kStageBytes);
-  uint64_t *kv_full = bars;                 // [kStages]
-  uint64_t *kv_empty = bars + kStages;      // [kStages]
-  uint64_t *s_full = bars + 2 * kStages;    // [2]
-  uint64_t *p_full = s_full + 2;            // [2]
-  uint64_t *pv_done = p_full + 2;           // [2], one per S/P buffer
-  uint64_t *q_full = pv_done + 2;
-  uint64_t *q_tmem = q_full + 1;
-  uint64_t *q_free = q_tmem + 1;
-  uint64_t *drain = q_free + 1;
-  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
-  volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
-
-  const int warp = warp_id(), lane = lane_id();
-  const int half = blockIdx.x & 1;
-  const int group = blockIdx.x >> 1;
-
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
-    }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
-    }
-    mbar_init(&pv_done[0], 1);
-    mbar_init(&pv_done[1], 1);
-    mbar_init(q_full, 1);
-    mbar_init(q_tmem, 128);
-    mbar_init(q_free, 1);
-    mbar_init(drain, 1);
-    *abort_flag = 0;
-    fence_barrier_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  // the prologue above overlaps the plan kernel; the plan is read below
-  grid_dep_wait();
-  grid_dep_launch();
-
-  SegWalk walk;
-  walk.init(args.plan, args.J, args.q_len, args.H, args.HG, args.groups, group, kTile);
-  Seg sg;
-
-  if (warp == 0) {
-    // -------------------------------------------------- TMA producer
-    // The whole warp walks the work; lane 0 issues barrier and TMA
-    // operations.  Block-table entries are fetched 32 pages at a time (one
-    // per lane) and broadcast with shuffles, so no tile waits on a global
-    // load.
-    if (lane == 0) {
-      prefetch_tmap(&tm_kv);
-      prefetch_tmap(&tm_q);
-    }
-    int kc = 0, nseg = 0;
-    bool ok = true;
-    while (ok && walk.next(sg)) {
-      const int32_t *bt = args.block_table + static_cast<int64_t>(sg.b) * args.max_blocks;
-      int page_base = -(1 << 30), my_blk = -1;
-      auto blk_of = [&](int tile) -> int {  // warp-collective
-        const int page = tile * kTile / kPage;
-        if (page < page_base || page >= page_base + 32) {
-          page_base = page;
-          my_blk = page + lane < args.max_blocks ? __ldg(bt + page + lane) : -1;
-        }
-        return __shfl_sync(0xffffffffu, my_blk, page - page_base);
-      };
-      auto row_of = [&](int tile, int blk) -> int {
-        return blk * kPage + (tile * kTile) % kPage;
-      };
-      // Loads KV tile `tile` into ring slot kc % kStages.
-      auto load_tile = [&](int tile) -> bool {
-        const int s = kc % kStages;
-        if (kc >= kStages && !mbar_wait(&kv_empty[s], ((kc / kStages) - 1) & 1, abort_flag))
-          return false;
-        const int blk = blk_of(tile);
-        if (lane == 0) {
-          int row;
-          if (blk < 0 || blk >= args.num_blocks) {
-            raise_error(args.err, MLA_DEVERR_BLOCK_ID);
-            row = args.num_blocks * kPage;  // out of range: TMA fills zeros
-          } else {
-            row = row_of(tile, blk);
-          }
-          uint8_t *dst = sm_kv + s * kStageBytes;
-          mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
-          for (int d = 0; d < 9; ++d)
-            tma_load_2d(dst + d * kBox, &tm_kv, &kv_full[s], 64 * d, row);
-        }
-        ++kc;
-        return true;
-      };
-      // The first ring-full of this segment's tiles only needs free ring
-      // slots; the query slot frees when the previous segment's MMAs end.
-      const int pre = min(sg.ntiles, kStages);
-      for (int t = 0; ok && t < pre; ++t) ok = load_tile(sg.tile0 + t);
-      if (!ok) break;
-      if (nseg > 0 && !(ok = mbar_wait(q_free, (nseg - 1) & 1, abort_flag))) break;
-      if (lane == 0) {
-        mbar_arrive_expect_tx(q_full, kQsBoxes * kQBox);
-        for (int k = 0; k < kQsBoxes; ++k)
-          tma_load_2d(sm_q + k * kQBox, &tm_q, q_full, kQsFirstCol + 64 * k, sg.row0);
-      }
-      ++nseg;
-      for (int t = pre; ok && t < sg.ntiles; ++t) ok = load_tile(sg.tile0 + t);
-    }
-    if (*abort_flag && lane == 0) {
-      volatile int no_abort = 0;
-      for (int k = max(0, kc - kStages); k < kc; ++k)
-        mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &no_abort);
-      if (nseg > 0) mbar_wait(q_full, (nseg - 1) & 1, &no_abort);
-    }
-  } else if (warp == 1) {
-    if (lane == 0) {
-      // ------------------------------------------------ MMA issuer
-      const uint32_t idesc_qk = FP8 ? idesc_e4m3(128, kTile, false, false)
-                                    : idesc_bf16(128, kTile, false, false);
-      const uint32_t idesc_pv = FP8 ? idesc_e4m3(128, 256, false, true)
-                                    : idesc_bf16(128, 256, false, true);
-      const uint32_t q_base = smem_u32(sm_q);
-      int kc = 0, uc = 0, nseg = 0;
-      bool ok = true;
-      // QK of one tile is issued in kQkChunks pieces so the MMA thread can
-      // slip PV(t) in between as soon as P(t) is ready (a single thread
-      // needs ~60 cycles per tcgen05.mma, ~2,300 for a whole bf16 QK).
-      constexpr int kQkChunks = 4;
-      constexpr int kChunkSteps = (kQkSteps + kQkChunks - 1) / kQkChunks;
-      // `chunk_c` is a std::integral_constant so every descriptor offset
-      // below is a compile-time constant.
-      auto issue_qk_chunk_c = [&](int kcx, int ucx, auto chunk_c) {
-        constexpr int chunk = decltype(chunk_c)::value;
-        const uint32_t stage = smem_u32(sm_kv + (kcx % kStages) * kStageBytes);
-        const uint32_t d = tmem + kColS + kTile * (ucx & 1);
-#pragma unroll
-        for (int j = 0; j < kChunkSteps; ++j) {
-          const int k = chunk * kChunkSteps + j;
-          if (k >= kQkSteps) break;
-          const uint32_t off = (k / kStepsPerBox) * kBox + (k % kStepsPerBox) * 32;
-          const uint64_t bdesc = sdesc(stage + off, 16, G::kSBO, G::kSwizzle);
-          if (k < kTmemQSteps) {
-            mma_f16_ts(d, tmem + G::kColQ + 8 * k, bdesc, idesc_qk, k > 0);
-          } else {
-            const int kq = k - kTmemQSteps;
-            const uint64_t adesc =
-                sdesc(q_base + (kq / kStepsPerBox) * kQBox + (kq % kStepsPerBox) * 32, 16,
-                      G::kSBO, G::kSwizzle);
-            if (FP8) mma_f8_ss(d, adesc, bdesc, idesc_qk, k > 0);
-            else mma_f16_ss(d, adesc, bdesc, idesc_qk, k > 0);
-          }
-        }
-        if (chunk == kQkChunks - 1) mma_commit(&s_full[ucx & 1]);
-      };
-      auto issue_qk_chunk = [&](int kcx, int ucx, int chunk) {
-        static_assert(kQkChunks == 4, "dispatch below covers four chunks");
-        switch (chunk) {
-          case 0: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 0>{}); break;
-          case 1: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 1>{}); break;
-          case 2: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 2>{}); break;
-          default: issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 3>{}); break;
-        }
-      };
-      auto issue_qk = [&](int kcx, int ucx) {
-        issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 0>{});
-        issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 1>{});
-        issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 2>{});
-        issue_qk_chunk_c(kcx, ucx, std::integral_constant<int, 3>{});
-      };
-      while (ok && walk.next(sg)) {
-        // the query of this segment: smem part by TMA, TMEM part by softmax warps
-        ok = mbar_wait(q_full, nseg & 1, abort_flag) &&
-             mbar_wait(q_tmem, nseg & 1, abort_flag);
-        if (!ok) break;
-        ++nseg;
-        ok = mbar_wait(&kv_full[kc % kStages], (kc / kStages) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        issue_qk(kc, uc);
-        for (int t = 0; t < sg.ntiles; ++t, ++kc, ++uc) {
-          // QK(t+1) and PV(t) are independent (different TMEM columns and
-          // inputs): PV(t) goes out as soon as P(t) is ready, between QK
-          // chunks if need be, so a ring slot is released without waiting
-          // for the next tile's MMAs; polling uses the non-blocking
-          // mbarrier test (try_wait may sleep until its barrier flips).
-          int chunks = t + 1 < sg.ntiles ? 0 : kQkChunks;   // QK(t+1) chunks issued
-          bool pv = false;
-          long long t_spin = 0;
-          while (!pv || chunks < kQkChunks) {
-            bool progressed = false;
-            if (!pv && mbar_test(&p_full[uc & 1], (uc >> 1) & 1)) {
-              tc_fence_after();
-              const uint32_t stage = smem_u32(sm_kv + (kc % kStages) * kStageBytes);
-#pragma unroll
-              for (int kk = 0; kk < kPvSteps; ++kk) {
-                // value half: boxes 4*half..4*half+3 (64 latent columns each),
-                // MN-major: N-blocks one box apart (LBO), 8-token groups SBO apart
-                const uint64_t bdesc = sdesc(stage + (4 * half) * kBox + kk * 2048, kBox,
-                                             G::kSBO, G::kSwizzle);
-                const uint32_t a = tmem + kColS + kTile * (uc & 1) + 8 * kk;
-                if (FP8) mma_f8_ts(tmem + kColO, a, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-                else mma_f16_ts(tmem + kColO, a, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
-              }
-              mma_commit(&kv_empty[kc % kStages]);
-              mma_commit(&pv_done[uc & 1]);
-              if (t + 1 == sg.ntiles) mma_commit(q_free);
-              pv = true;
-              progressed = true;
-            }
-            if (chunks < kQkChunks &&
-                (chunks > 0 || mbar_test(&kv_full[(kc + 1) % kStages], ((kc + 1) / kStages) & 1))) {
-              if (chunks == 0) tc_fence_after();
-              issue_qk_chunk(kc + 1, uc + 1, chunks);
-              ++chunks;
-              progressed = true;
-            }
-            if (progressed) continue;
-            if (*abort_flag) break;
-            if (t_spin == 0) t_spin = clock64();
-            else if (clock64() - t_spin > kWaitLimitCycles) { *abort_flag = 1; break; }
-          }
-          if (!pv || chunks < kQkChunks) { ok = false; break; }
-        }
-      }
-      if (!ok) {
-        mma_commit(drain);
-        volatile int no_abort = 0;
-        mbar_wait(drain, 0, &no_abort);
-      }
-    }
-  } else {
-    // -------------------------------------------- softmax / epilogue
-    const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // head row within the group
-    const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
-    const int tid = threadIdx.x - 64;   // 0..127
-    int uc = 0;
-    bool ok = true;
-    // Query dims [0, 2*kQtCols) of row r of segment `seg` -> TMEM columns
-    // [kColQ, kColQ + kQtCols) (two bf16 per 32-bit column).
-    // Done for the next segment as soon as the previous one's MMAs are over
-    // (before its epilogue), so the next QK MMAs overlap that epilogue.
-    auto load_q_tmem = [&](const Seg &seg) {
-      if (G::kQtCols > 0) {
-        const uint4 *src = reinterpret_cast<const uint4 *>(
-            args.q + static_cast<int64_t>(seg.row0 + r) * kDqk * 2);
-        const bool valid = r < seg.hrows;
-        // batches of 16 independent 16-byte loads (two TMEM stores each)
-#pragma unroll 1
-        for (int c = 0; c < G::kQtCols / 64; ++c) {
-          uint32_t w[64];
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            uint4 v = valid ? __ldg(src + c * 16 + k) : make_uint4(0, 0, 0, 0);
-            w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
-          }
-          tmem_st_x32(lane_base + G::kColQ + 64 * c, w);
-          tmem_st_x32(lane_base + G::kColQ + 64 * c + 32, w + 32);
-        }
-        tc_fence_before();
-      }
-      mbar_arrive(q_tmem);
-    };
-    bool have = walk.next(sg);
-    if (have) load_q_tmem(sg);
-    while (ok && have) {
-      float m = -INFINITY, l = 0.f, lq = 0.f;
-      const int len = __ldg(args.seq_lens + sg.b);
-      for (int t = 0; t < sg.ntiles; ++t, ++uc) {
-        const int sb = uc & 1;
-        ok = mbar_wait(&s_full[sb], (uc >> 1) & 1, abort_flag);
-        if (!ok) break;
-        tc_fence_after();
-        const int pos0 = (sg.tile0 + t) * kTile;
-        float x[kTile];
-        float tmax = -INFINITY;
-        // interior tiles (every position inside [lo, hi)) skip the mask
-        const bool full_tile = pos0 >= sg.lo && pos0 + kTile <= sg.hi;
-#pragma unroll
-        for (int c = 0; c < kTile; c += 32) {
-          uint32_t sr[32];
-          tmem_ld_x32(lane_base + kColS + kTile * sb + c, sr);
-          if (full_tile) {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              x[c + jj] = __uint_as_float(sr[jj]) * args.scale_log2;
-              tmax = fmaxf(tmax, x[c + jj]);
-            }
-          } else {
-#pragma unroll
-            for (int jj = 0; jj < 32; ++jj) {
-              const int pos = pos0 + c + jj;
-              const bool valid = pos >= sg.lo && pos < sg.hi;
-              x[c + jj] = valid ? __uint_as_float(sr[jj]) * args.scale_log2 : -INFINITY;
-              tmax = fmaxf(tmax, x[c + jj]);
-            }
-          }
-        }
-        if (t > 0) {
-          const float m_new = fmaxf(m, tmax);
-          const bool need = m_new > m + kRescaleLog2;
-          if (__any_sync(0xffffffffu, need)) {
-            // O may only be rescaled once PV(t-1) has landed.  PV completions
-            // are committed to the barrier of their S/P buffer, so the
-            // barrier of tile t-1 is at most one phase ahead of this wait
-            // and skipped waits on tiles without a rescale are harmless.
-            const int up = uc - 1;
-            ok = mbar_wait(&pv_done[up & 1], (up >> 1) & 1, abort_flag);
-            if (!ok) break;
-            tc_fence_after();
-            const float alpha = need ? ex2(m - m_new) : 1.f;
-#pragma unroll 1
-            for (int c = 0; c < 256; c += 32) {
-              uint32_t o[32];
-              tmem_ld_x32(lane_base + kColO + c, o);
-#pragma unroll
-              for (int k = 0; k < 32; ++k)
-                o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-              tmem_st_x32(lane_base + kColO + c, o);
-            }
-            l *= alpha;
-            lq *= alpha;
-            if (need) m = m_new;
-          }
-        } else {
-          m = tmax;
-        }
-        // Two row sums: `l` of the unrounded fp32 probabilities gives the
-        // LSE (no rounding of P in it); `lq` of the rounded values that the
-        // P.V MMA actually consumes normalises O, so O stays a convex
-        // combination of the value rows.
-#pragma unroll
-        for (int k = 0; k < kTile; ++k) x[k] = ex2(x[k] - m);
-        float psum = 0.f, qsum = 0.f;
-#pragma unroll
-        for (int k = 0; k < kTile; ++k) psum += x[k];
-        l += psum;
-        constexpr int kPCols = FP8 ? kTile / 4 : kTile / 2;   // 32-bit TMEM columns of P
-        uint32_t pk[kPCols];
-        if (FP8) {
-#pragma unroll
-          for (int k = 0; k < kPCols; ++k) {
-            pk[k] = pack_e4m3x4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
-            __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
-                static_cast<__nv_fp8x2_storage_t>(pk[k] & 0xFFFFu), __NV_E4M3);
-            __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(
-                static_cast<__nv_fp8x2_storage_t>(pk[k] >> 16), __NV_E4M3);
-            const float2 f0 = __half22float2(*reinterpret_cast<__half2 *>(&h0));
-            const float2 f1 = __half22float2(*reinterpret_cast<__half2 *>(&h1));
-            qsum += (f0.x + f0.y) + (f1.x + f1.y);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < kPCols; ++k) {
-            pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
-            qsum += __uint_as_float(pk[k] << 16) + __uint_as_float(pk[k] & 0xFFFF0000u);
-          }
-        }
-        lq += qsum;
-        if (kPCols == 32) tmem_st_x32(lane_base + kColS + kTile * sb, pk);
-        else tmem_st_x16(lane_base + kColS + kTile * sb, pk);
-        if (pos0 + kTile > len) {
-          // Cache rows past seq_len may hold anything (even NaN bits): zero
-          // this CTA's value columns of those rows so that P = 0 really
-          // contributes nothing to O.  The tile sits in ring stage
-          // uc % kStages (the producer fills stages in the same order).
-          const int first = max(0, len - pos0);
-          const int nrows = kTile - first;
-          constexpr int kChunks = G::kRowBytes / 16;
-          uint8_t *vbase = sm_kv + (uc % kStages) * kStageBytes + (4 * half) * kBox;
-          for (int idx = tid; idx < nrows * 4 * kChunks; idx += 128) {
-            const int box = idx / (nrows * kChunks);
-            const int rem = idx - box * nrows * kChunks;
-            reinterpret_cast<uint4 *>(vbase + box * kBox +
-                                      (first + rem / kChunks) * G::kRowBytes)[rem % kChunks] =
-                make_uint4(0, 0, 0, 0);
-          }
-          fence_proxy_async_smem();
-        }
-        tc_fence_before();
-        mbar_arrive(&p_full[sb]);
-      }
-      if (!ok) break;
-      {
-        const int up = uc - 1;  // the last PV of this segment (all earlier ones are done too)
-        ok = mbar_wait(&pv_done[up & 1], (up >> 1) & 1, abort_flag);
-      }
-      if (!ok) break;
-      tc_fence_after();
-      // every MMA of this segment is done: stage the next segment's query
-      const Seg cur = sg;
-      have = walk.next(sg);
-      if (have) load_q_tmem(sg);
-      // ---- epilogue: O / l for this CTA's 256 latent columns
-      const float inv = args.out_scale / lq;
-      const bool row_ok = r < cur.hrows;
-      const int64_t orow = static_cast<int64_t>(cur.out_row0 + r);
-#pragma unroll 1
-      for (int c = 0; c < 256; c += 32) {
-        uint32_t o[32];
-        tmem_ld_x32(lane_base + kColO + c, o);
-        if (!row_ok) continue;
-        float v[32];
-#pragma unroll
-        for (int k = 0; k < 32; ++k) v[k] = __uint_as_float(o[k]) * inv;
-        const int col = 256 * half + c;
-        if (args.out_dtype == MLA_BF16) {
-          // partials take the output's type
-          __nv_bfloat16 *base =
-              cur.whole ? static_cast<__nv_bfloat16 *>(args.out) + orow * kLatent + col
-                        : reinterpret_cast<__nv_bfloat16 *>(args.ws_o) +
-                              (static_cast<int64_t>(cur.slot) * 128 + r) * kLatent + col;
-          uint4 *dst = reinterpret_cast<uint4 *>(base);
-#pragma unroll
-          for (int k = 0; k < 4; ++k)
-            dst[k] = make_uint4(pack_bf16(v[8 * k], v[8 * k + 1]),
-                                pack_bf16(v[8 * k + 2], v[8 * k + 3]),
-                                pack_bf16(v[8 * k + 4], v[8 * k + 5]),
-                                pack_bf16(v[8 * k + 6], v[8 * k + 7]));
-        } else {
-          float *base = cur.whole
-                            ? static_cast<float *>(args.out) + orow * kLatent + col
-                            : args.ws_o + (static_cast<int64_t>(cur.slot) * 128 + r) * kLatent + col;
-          float4 *dst = reinterpret_cast<float4 *>(base);
-#pragma unroll
-          for (int k = 0; k < 8; ++k)
-            dst[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
-        }
-      }
-      if (row_ok && half == 0) {
-        const float lse = (m + log2f(l)) * 0.69314718055994531f;
-        if (cur.whole) args.lse[orow] = lse;
-        else args.ws_lse[static_cast<int64_t>(cur.slot) * 128 + r] = lse;
-      }
-      tc_fence_before();
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0 && *abort_flag) raise_error(args.err, MLA_DEVERR_TIMEOUT);
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 512);
-  }
-}
-
-// ------------------------------------------------ bf16 split-QK pair kernel
+// ------------------------------------------------- split-QK pair kernel
 // The two CTAs of a 2-CTA cluster share one work span.  CTA c loads only
 // latent columns [256c, 256c + 256) of each KV tile plus rope columns
-// [32c, 32c + 32) (36 KB instead of 72 KB per tile) and computes the
+// [32c, 32c + 32) (36 KB instead of 72 KB per bf16 tile) and computes the
 // partial scores of its 288 columns (16 latent K steps with the query in
 // TMEM, 2 rope K steps with the query rope half in shared memory).  The
 // partials are summed across the pair through distributed shared memory:
@@ -1003,26 +457,64 @@ constexpr int kOffSRecv = kOffSSend + kSMsg;
 constexpr int kOffAlSend = kOffSRecv + kSMsg;                 // [2]
 constexpr int kOffAlRecv = kOffAlSend + 2 * kAlMsg;           // [2]
 constexpr int kOffBars = kOffAlRecv + 2 * kAlMsg;
-constexpr int kNumBars = 2 * kStages + 28;
+constexpr int kMaxStages = 8;                   // ring stages of the e4m3 format
+constexpr int kNumBars = 2 * kMaxStages + 28;
 constexpr int kSegSlots = 4;                    // segment descriptors in flight
 constexpr int kOffSegQ = kOffBars + kNumBars * 8 + 16;
 constexpr int kSmem = kOffSegQ + kSegSlots * 64 + 1024;
-constexpr int kQkChunks = 3;
-constexpr int kChunkSteps = 6;                  // 18 K=16 steps: 16 latent + 2 rope
-constexpr int kPvSteps = kTile / 16;
-constexpr uint32_t kColQ = 384;                 // query latent half, 128 columns
-constexpr uint32_t kPMsg = 64 * 128 + kAlMsg;   // bytes landing per P message
+constexpr int kQkChunks = 3;                    // QK of a tile in three bursts
+constexpr uint32_t kColQ = 384;                 // query latent half (128 / 64 columns)
 static_assert(kSmem <= 232448, "shared memory of one CTA");
 static_assert(kOffP % 1024 == 0 && kOffQ % 1024 == 0 && kStageBytes % 1024 == 0,
               "swizzled tiles start on 1024-byte boundaries");
+
+// What differs between the bf16 and the e4m3 cache.  Either way a CTA loads
+// four latent boxes of 64 columns x 64 tokens and one rope box of 32
+// columns (its half), every QK K step covers 32 bytes of a row (16 bf16 or
+// 32 e4m3: eight 32-bit TMEM columns of the query), and a P.V K step covers
+// 2 KB of the value boxes (16 tokens x 128 B or 32 tokens x 64 B), so the
+// shared-memory layout above holds both (e4m3 stages are half as large,
+// twice as many fill the ring; its P rows are 64 B).
+template <bool FP8>
+struct Fmt {
+  static constexpr int kEsz = FP8 ? 1 : 2;                 // bytes per element
+  static constexpr int kBox = 64 * 64 * kEsz;              // latent box
+  static constexpr int kRopeBox = 64 * 32 * kEsz;          // rope box
+  static constexpr int kStageBytes = 4 * kBox + kRopeBox;  // 18 / 36 KB
+  static constexpr int kStages = (4 * 36864) / kStageBytes;   // 8 / 4: the same ring bytes
+  static constexpr int kQRopeBytes = 128 * 32 * kEsz;
+  static constexpr uint32_t kSwL = FP8 ? sm100::kSwizzle64B : sm100::kSwizzle128B;
+  static constexpr uint32_t kSwR = FP8 ? sm100::kSwizzle32B : sm100::kSwizzle64B;
+  static constexpr uint32_t kSboL = 8 * 64 * kEsz;         // 8 rows of a latent box
+  static constexpr uint32_t kSboR = 8 * 32 * kEsz;         // 8 rows of a rope box
+  static constexpr int kStepsPerBox = 64 * kEsz / 32;      // QK K steps per box row
+  static constexpr int kLatSteps = 4 * kStepsPerBox;       // 8 / 16
+  static constexpr int kRopeSteps = 32 * kEsz / 32;        // 1 / 2
+  static constexpr int kChunkSteps = (kLatSteps + kRopeSteps) / 3;   // 3 / 6
+  static constexpr int kPvSteps = FP8 ? 2 : 4;             // 32 / 16 tokens per step
+  static constexpr int kPRow = 64 * kEsz;                  // bytes of one P row
+  static constexpr uint32_t kSwP = FP8 ? sm100::kSwizzle64B : sm100::kSwizzle128B;
+  static constexpr uint32_t kSboP = 8 * kPRow;
+  static constexpr uint32_t kPMsg = 64 * kPRow + kAlMsg;   // bytes landing per P message
+  static constexpr int kQCols = 64 * kEsz;                 // TMEM columns of the query half
+  static_assert(kStages <= kMaxStages && kStages * kStageBytes == 4 * 36864, "ring");
+  static_assert(3 * kChunkSteps == kLatSteps + kRopeSteps, "three QK chunks");
+};
 }  // namespace pair
 
+template <bool FP8>
 __global__ void __launch_bounds__(pair::kThreads, 1)
 decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                    const __grid_constant__ CUtensorMap tm_kr,
                    const __grid_constant__ CUtensorMap tm_qr,
                    DecodeArgs args) {
   using namespace pair;
+  using F = Fmt<FP8>;
+  // the format's geometry under the names the code below uses
+  constexpr int kStages = F::kStages, kStageBytes = F::kStageBytes, kBox = F::kBox;
+  constexpr int kQRopeBytes = F::kQRopeBytes, kPvSteps = F::kPvSteps;
+  constexpr int kChunkSteps = F::kChunkSteps;
+  constexpr uint32_t kPMsg = F::kPMsg;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -1211,8 +703,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           // rows (contiguous) are pulled into L2 here, in a few large
           // prefetches (many small ones would hold up the TMA loads behind
           // them).
-          const uint8_t *qrows = args.q + static_cast<int64_t>(sg.row0) * kDqk * 2;
-          const uint32_t bytes = static_cast<uint32_t>(sg.hrows) * kDqk * 2;
+          const uint8_t *qrows = args.q + static_cast<int64_t>(sg.row0) * kDqk * F::kEsz;
+          const uint32_t bytes = static_cast<uint32_t>(sg.hrows) * kDqk * F::kEsz;
           for (uint32_t o = 0; o < bytes; o += 16384)
             prefetch_l2(qrows + o, min(16384u, bytes - o));
         }
@@ -1230,8 +722,10 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
   } else if (is_mma) {
     if (lane == 0) {
       // ------------------------------------------------ MMA issuer
-      const uint32_t idesc_qk = idesc_bf16(128, kTile, false, false);
-      const uint32_t idesc_pv = idesc_bf16(128, 256, false, true);
+      const uint32_t idesc_qk = FP8 ? idesc_e4m3(128, kTile, false, false)
+                                    : idesc_bf16(128, kTile, false, false);
+      const uint32_t idesc_pv = FP8 ? idesc_e4m3(128, 256, false, true)
+                                    : idesc_bf16(128, 256, false, true);
       const uint32_t q_base = smem_u32(sm_q);
       int kc = 0, uc = 0, nseg = 0;
       bool ok = true;
@@ -1244,15 +738,18 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
 #pragma unroll
         for (int j = 0; j < kChunkSteps; ++j) {
           const int k = chunk * kChunkSteps + j;
-          if (k < 16) {   // latent: A = query half in TMEM, B = own latent boxes
-            const uint64_t bdesc = sdesc(stage + (k / 4) * kBox + (k % 4) * 32, 16, 1024,
-                                         kSwizzle128B);
-            mma_f16_ts(d, tmem + kColQ + 8 * k, bdesc, idesc_qk, k > 0 ? 1u : 0u);
-          } else {        // rope: this CTA's 32 rope columns, two K steps
-            const int kk = k - 16;
-            const uint64_t bdesc = sdesc(stage + 4 * kBox + kk * 32, 16, 512, kSwizzle64B);
-            const uint64_t adesc = sdesc(q_base + kk * 32, 16, 512, kSwizzle64B);
-            mma_f16_ss(d, adesc, bdesc, idesc_qk, 1u);
+          if (k < F::kLatSteps) {   // latent: A = query half in TMEM, B = own latent boxes
+            const uint64_t bdesc =
+                sdesc(stage + (k / F::kStepsPerBox) * kBox + (k % F::kStepsPerBox) * 32, 16,
+                      F::kSboL, F::kSwL);
+            if constexpr (FP8) mma_f8_ts(d, tmem + kColQ + 8 * k, bdesc, idesc_qk, k > 0 ? 1u : 0u);
+            else mma_f16_ts(d, tmem + kColQ + 8 * k, bdesc, idesc_qk, k > 0 ? 1u : 0u);
+          } else {                  // rope: this CTA's 32 rope columns
+            const int kk = k - F::kLatSteps;
+            const uint64_t bdesc = sdesc(stage + 4 * kBox + kk * 32, 16, F::kSboR, F::kSwR);
+            const uint64_t adesc = sdesc(q_base + kk * 32, 16, F::kSboR, F::kSwR);
+            if constexpr (FP8) mma_f8_ss(d, adesc, bdesc, idesc_qk, 1u);
+            else mma_f16_ss(d, adesc, bdesc, idesc_qk, 1u);
           }
         }
         if (chunk == kQkChunks - 1) {
@@ -1310,12 +807,15 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           const uint32_t pbuf = smem_u32(sm_p + (uc & 1) * kPBuf);
 #pragma unroll
           for (int kk = 0; kk < kPvSteps; ++kk) {
-            // A = P (K-major, 16 tokens per step); B = the four own latent
-            // boxes, MN-major: N-blocks one box apart (LBO), 8-token
-            // groups SBO apart
-            const uint64_t adesc = sdesc(pbuf + kk * 32, 16, 1024, kSwizzle128B);
-            const uint64_t bdesc = sdesc(stage + kk * 2048, kBox, 1024, kSwizzle128B);
-            mma_f16_ss(tmem + kColO, adesc, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+            // A = P (K-major, 32 bytes of tokens per step); B = the four own
+            // latent boxes, MN-major: N-blocks one box apart (LBO), 8-token
+            // groups SBO apart, 2 KB of rows per step
+            const uint64_t adesc = sdesc(pbuf + kk * 32, 16, F::kSboP, F::kSwP);
+            const uint64_t bdesc = sdesc(stage + kk * 2048, kBox, F::kSboL, F::kSwL);
+            if constexpr (FP8)
+              mma_f8_ss(tmem + kColO, adesc, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
+            else
+              mma_f16_ss(tmem + kColO, adesc, bdesc, idesc_pv, (t > 0 || kk > 0) ? 1u : 0u);
           }
           mma_commit(&kv_empty[kc % kStages]);
           mma_commit(&pv_done[uc & 1]);
@@ -1397,22 +897,23 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     // warp-collective operation is left waiting for a lane that has gone
     auto warp_ok = [](bool v) { return __all_sync(0xffffffffu, v); };
     // Query latent dims [256*half, 256*half + 256) of row r -> TMEM columns
-    // [kColQ, kColQ + 128), two bf16 per 32-bit column.
+    // [kColQ, kColQ + F::kQCols): two bf16 or four e4m3 per 32-bit column.
     auto load_q_tmem = [&](const Seg &seg) {
+      constexpr int kVec = F::kQCols / 4;   // 16-byte loads per row half
       const uint4 *src = reinterpret_cast<const uint4 *>(
-                             args.q + static_cast<int64_t>(seg.row0 + r) * kDqk * 2) +
-                         32 * half;
+                             args.q + static_cast<int64_t>(seg.row0 + r) * kDqk * F::kEsz) +
+                         kVec * half;
       const bool valid = r < seg.hrows;
-      // all 32 loads in flight at once: under the KV stream every round
-      // trip to memory costs thousands of cycles
-      uint32_t w[128];
+      // all loads in flight at once: under the KV stream every round trip
+      // to memory costs thousands of cycles
+      uint32_t w[F::kQCols];
 #pragma unroll
-      for (int k = 0; k < 32; ++k) {
+      for (int k = 0; k < kVec; ++k) {
         uint4 v = valid ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
         w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
       }
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_st_x32(lane_base + kColQ + 32 * c, w + 32 * c);
+      for (int c = 0; c < F::kQCols / 32; ++c) tmem_st_x32(lane_base + kColQ + 32 * c, w + 32 * c);
       tc_fence_before();
       mbar_arrive(q_tmem);
     };
@@ -1437,7 +938,8 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     bool have_next = false;
     float l_in = 1.f;   // forwarded rows: the owner's running sum, last message
     while (ok && have) {
-      float m = -INFINITY, l = 0.f;
+      // running max and sum; lq (e4m3) sums the rounded probabilities
+      float m = -INFINITY, l = 0.f, lq = 0.f;
       const int len = sg.len;
       for (int t = 0; t < sg.ntiles; ++t, ++uc) {
         const int sb = uc & 1;
@@ -1507,6 +1009,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                 tmem_st_x32(lane_base + kColO + c, o);
               }
               l *= alpha;
+              lq *= alpha;
               if (need) m = m_new;
             }
           } else {
@@ -1529,9 +1032,29 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
             add_f32x2(ps[2], ps[3], ps[2], ps[3], x[k + 2], x[k + 3]);
           }
           l += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-          uint32_t pk[kTile / 2];
+          // P for the P.V operand: bf16 pairs, or e4m3 quads, whose rounding
+          // is coarse enough that O is normalised by the sum of the rounded
+          // values (lq) while the LSE keeps the unrounded sum
+          constexpr int kPk = FP8 ? kTile / 4 : kTile / 2;
+          uint32_t pk[kPk];
+          if constexpr (FP8) {
+            float qs[2] = {0.f, 0.f};
 #pragma unroll
-          for (int k = 0; k < kTile / 2; ++k) pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
+            for (int k = 0; k < kPk; ++k) {
+              pk[k] = pack_e4m3x4(x[4 * k], x[4 * k + 1], x[4 * k + 2], x[4 * k + 3]);
+              __half2_raw h0 = __nv_cvt_fp8x2_to_halfraw2(
+                  static_cast<__nv_fp8x2_storage_t>(pk[k] & 0xFFFFu), __NV_E4M3);
+              __half2_raw h1 = __nv_cvt_fp8x2_to_halfraw2(
+                  static_cast<__nv_fp8x2_storage_t>(pk[k] >> 16), __NV_E4M3);
+              const float2 f0 = __half22float2(*reinterpret_cast<__half2 *>(&h0));
+              const float2 f1 = __half22float2(*reinterpret_cast<__half2 *>(&h1));
+              qs[k & 1] += (f0.x + f0.y) + (f1.x + f1.y);
+            }
+            lq += qs[0] + qs[1];
+          } else {
+#pragma unroll
+            for (int k = 0; k < kPk; ++k) pk[k] = pack_bf16(x[2 * k], x[2 * k + 1]);
+          }
           // P tile `sb` and the factor slot are free once P.V of tile uc-2
           // is done here (and the copy out of them has landed) and in the
           // peer (which takes our rows into its own P tile)
@@ -1541,23 +1064,27 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                          mbar_wait(&pb_free[sb], (up >> 1) & 1, abort_flag));
             if (!ok) break;
           }
-          // row r of the K-major, 128B-swizzled P operand: 8 chunks of 8 tokens
-          uint4 *prow = reinterpret_cast<uint4 *>(pbuf + r * 128);
+          // row r of the K-major P operand: 8 chunks of 8 bf16 tokens,
+          // 128B-swizzled, or 4 chunks of 16 e4m3 tokens, 64B-swizzled (the
+          // 16-byte chunk index XOR the address bits above the row pair)
+          uint4 *prow = reinterpret_cast<uint4 *>(pbuf + r * F::kPRow);
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            prow[j ^ (r & 7)] = make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
-          // factors of this warp's rows: alpha[32] then the running sum l[32]
+          for (int j = 0; j < kPk / 4; ++j)
+            prow[FP8 ? (j ^ ((r >> 1) & 3)) : (j ^ (r & 7))] =
+                make_uint4(pk[4 * j], pk[4 * j + 1], pk[4 * j + 2], pk[4 * j + 3]);
+          // factors of this warp's rows: alpha[32] then the normaliser of O
+          // (the running sum l, or lq for e4m3 P) [32]
           float *al = reinterpret_cast<float *>(al_send + sb * kAlMsg + wl * (kAlMsg / 2));
           al[lane] = alpha;
-          al[32 + lane] = l;
+          al[32 + lane] = FP8 ? lq : l;
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) {
             // this warp's 32 rows of P (contiguous) and their factors -> the
             // same places in the peer
             const uint32_t xbar = peer_smem(&xp_full[sb], peer);
-            uint8_t *rows = pbuf + (64 * half + 32 * wl) * 128;
-            bulk_copy_to_peer(peer_smem(rows, peer), rows, 32 * 128, xbar);
+            uint8_t *rows = pbuf + (64 * half + 32 * wl) * F::kPRow;
+            bulk_copy_to_peer(peer_smem(rows, peer), rows, 32 * F::kPRow, xbar);
             uint8_t *al_dst = al_recv + sb * kAlMsg + wl * (kAlMsg / 2);
             bulk_copy_to_peer(peer_smem(al_dst, peer), al, kAlMsg / 2, xbar);
           }
@@ -1600,11 +1127,13 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           // them in this CTA's value boxes so that P = 0 contributes nothing
           const int first = max(0, len - pos0);
           const int nrows = kTile - first;
+          // (every 16-byte chunk of a row: the swizzle only permutes them)
+          constexpr int kCh = 4 * F::kEsz;   // 16-byte chunks per box row
           uint8_t *vbase = sm_kv + (uc % kStages) * kStageBytes;
-          for (int idx = tid; idx < nrows * 4 * 8; idx += 128) {
-            const int box = idx / (nrows * 8);
-            const int rem = idx - box * nrows * 8;
-            reinterpret_cast<uint4 *>(vbase + box * kBox + (first + rem / 8) * 128)[rem % 8] =
+          for (int idx = tid; idx < nrows * 4 * kCh; idx += 128) {
+            const int box = idx / (nrows * kCh);
+            const int rem = idx - box * nrows * kCh;
+            reinterpret_cast<uint4 *>(vbase + box * kBox + (first + rem / kCh) * 16 * kCh)[rem % kCh] =
                 make_uint4(0, 0, 0, 0);
           }
           fence_proxy_async_smem();
@@ -1645,7 +1174,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       // store instruction.  Nothing waits on the stores; tensor-map stores
       // from the same buffers would wait for the TMA engine to read each
       // one, behind the next segment's KV loads (~3.5 us per epilogue).
-      const float inv = args.out_scale / (own ? l : l_in);
+      const float inv = args.out_scale / (own ? (FP8 ? lq : l) : l_in);
       const bool row_ok = r < cur.hrows;
       // partials take the output's type (a bf16 output is rounded to bf16
       // anyway; the merge adds at most half a bf16 step of each part)
@@ -1760,7 +1289,7 @@ decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
   using G = mrg::Geo<Tout>;
   constexpr int kRing = G::kRing, kPartBytes = G::kPartBytes, kPartElems = G::kPartElems;
   constexpr int kOffLse = G::kOffLse, kOffBars = G::kOffBars;
-  extern __shared__ __align__(128) uint8_t smem_raw[];
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~uintptr_t(127));
   Tout *parts = reinterpret_cast<Tout *>(smem);
@@ -1924,10 +1453,11 @@ int groups_for_device() {
   std::lock_guard<std::mutex> lock(mu);
   if (cache[dev] > 0) return cache[dev];
   int clusters = 0;
-  if (cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  // (the two formats' kernels have the same launch shape and shared memory)
+  if (cudaFuncSetAttribute(decode_pair_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            pair::kSmem) == cudaSuccess) {
     PairLaunch pl(g, nullptr);
-    if (cudaOccupancyMaxActiveClusters(&clusters, decode_pair_kernel, &pl.cfg) != cudaSuccess)
+    if (cudaOccupancyMaxActiveClusters(&clusters, decode_pair_kernel<false>, &pl.cfg) != cudaSuccess)
       clusters = 0;
   }
   cudaGetLastError();   // a failed query leaves no sticky error behind
@@ -1972,7 +1502,7 @@ extern "C" int mla_decode_plan(const int32_t *seq_lens, const int32_t *kv_starts
   const int g = n_groups > 0 ? n_groups : groups_for_device();
   int *err = device_error_word();
   if (!err) return MLA_ERR_CUDA;
-  const int tile = kv_dtype == MLA_E4M3 ? Geo<true>::kTile : Geo<false>::kTile;
+  const int tile = pair::kTile;   // both formats
   if (launch_plan(seq_lens, kv_starts, kv_ends, B, q_len, HG, max_blocks, causal ? 1 : 0, tile,
                   split_tiles, g, plan, err, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
@@ -1982,60 +1512,32 @@ extern "C" int mla_decode_plan(const int32_t *seq_lens, const int32_t *kv_starts
 namespace {
 
 template <bool FP8>
-int launch_decode(const void *q, const void *kv_cache, int B, int q_len, int H,
-                  int num_blocks, DecodeArgs a, mla_stream_t stream) {
-  using G = Geo<FP8>;
-  const CUtensorMapDataType dt =
-      FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const CUtensorMapSwizzle sw = FP8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-  const uint64_t row_bytes = static_cast<uint64_t>(kDqk) * (FP8 ? 1 : 2);
-  CUtensorMap tm_kv, tm_q;
-  {
-    const uint64_t dims[2] = {kDqk, static_cast<uint64_t>(num_blocks) * kPage};
-    const uint64_t strides[1] = {row_bytes};
-    const uint32_t box[2] = {64, static_cast<uint32_t>(G::kTile)};
-    if (!make_tmap(&tm_kv, dt, 2, kv_cache, dims, strides, box, sw)) return MLA_ERR_CUDA;
-  }
-  {
-    const uint64_t dims[2] = {kDqk, static_cast<uint64_t>(B) * q_len * H};
-    const uint64_t strides[1] = {row_bytes};
-    const uint32_t box[2] = {64, 128};
-    if (!make_tmap(&tm_q, dt, 2, q, dims, strides, box, sw)) return MLA_ERR_CUDA;
-  }
-  constexpr int smem = smem_bytes<FP8>();
-  if (cudaFuncSetAttribute(decode_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           smem) != cudaSuccess)
-    return MLA_ERR_CUDA;
-  if (launch_pdl(decode_kernel<FP8>, dim3(2 * a.groups), dim3(kThreads), smem, stream,
-                 tm_kv, tm_q, a) != cudaSuccess)
-    return MLA_ERR_CUDA;
-  return MLA_OK;
-}
-
 int launch_decode_pair(const void *q, const void *kv_cache, int B, int q_len, int H,
                        int num_blocks, DecodeArgs a, mla_stream_t stream) {
-  // KV latent boxes {64 columns, 64 tokens} (128B swizzle); KV and query
-  // rope halves {32 columns, 64 tokens / 128 heads} (64B swizzle)
+  // KV latent boxes {64 columns, 64 tokens} (128B swizzle for bf16, 64B for
+  // e4m3: one box row either way); KV and query rope halves {32 columns,
+  // 64 tokens / 128 heads} (64B / 32B swizzle)
   CUtensorMap tm_kv, tm_kr, tm_qr;
-  const uint64_t row_bytes = static_cast<uint64_t>(kDqk) * 2;
+  const CUtensorMapDataType dt =
+      FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const CUtensorMapSwizzle sw_l = FP8 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
+  const CUtensorMapSwizzle sw_r = FP8 ? CU_TENSOR_MAP_SWIZZLE_32B : CU_TENSOR_MAP_SWIZZLE_64B;
+  const uint64_t row_bytes = static_cast<uint64_t>(kDqk) * pair::Fmt<FP8>::kEsz;
   const uint64_t kv_dims[2] = {kDqk, static_cast<uint64_t>(num_blocks) * kPage};
   const uint64_t q_dims[2] = {kDqk, static_cast<uint64_t>(B) * q_len * H};
   const uint64_t strides[1] = {row_bytes};
   const uint32_t box_kv[2] = {64, static_cast<uint32_t>(pair::kTile)};
   const uint32_t box_kr[2] = {32, static_cast<uint32_t>(pair::kTile)};
   const uint32_t box_qr[2] = {32, 128};
-  if (!make_tmap(&tm_kv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, kv_dims, strides, box_kv,
-                 CU_TENSOR_MAP_SWIZZLE_128B) ||
-      !make_tmap(&tm_kr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, kv_cache, kv_dims, strides, box_kr,
-                 CU_TENSOR_MAP_SWIZZLE_64B) ||
-      !make_tmap(&tm_qr, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, q, q_dims, strides, box_qr,
-                 CU_TENSOR_MAP_SWIZZLE_64B))
+  if (!make_tmap(&tm_kv, dt, 2, kv_cache, kv_dims, strides, box_kv, sw_l) ||
+      !make_tmap(&tm_kr, dt, 2, kv_cache, kv_dims, strides, box_kr, sw_r) ||
+      !make_tmap(&tm_qr, dt, 2, q, q_dims, strides, box_qr, sw_r))
     return MLA_ERR_CUDA;
-  if (cudaFuncSetAttribute(decode_pair_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (cudaFuncSetAttribute(decode_pair_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            pair::kSmem) != cudaSuccess)
     return MLA_ERR_CUDA;
   PairLaunch pl(a.groups, stream);
-  if (cudaLaunchKernelEx(&pl.cfg, decode_pair_kernel, tm_kv, tm_kr, tm_qr, a) !=
+  if (cudaLaunchKernelEx(&pl.cfg, decode_pair_kernel<FP8>, tm_kv, tm_kr, tm_qr, a) !=
       cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
@@ -2101,7 +1603,7 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   float *ws_o = reinterpret_cast<float *>(ws + w.o_off);
   float *ws_lse = reinterpret_cast<float *>(ws + w.lse_off);
 
-  const int tile = fp8 ? Geo<true>::kTile : Geo<false>::kTile;
+  const int tile = pair::kTile;   // both formats
   if (launch_plan(seq_lens, kv_starts, kv_ends, B, q_len, HG, max_blocks, causal ? 1 : 0, tile,
                   split_tiles, g, plan, err, stream) != cudaSuccess)
     return MLA_ERR_CUDA;
@@ -2126,8 +1628,8 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
   a.ws_o = ws_o;
   a.ws_lse = ws_lse;
   a.err = err;
-  const int st = fp8 ? launch_decode<true>(q, kv_cache, B, q_len, H, num_blocks, a, stream)
-                     : launch_decode_pair(q, kv_cache, B, q_len, H, num_blocks, a, stream);
+  const int st = fp8 ? launch_decode_pair<true>(q, kv_cache, B, q_len, H, num_blocks, a, stream)
+                     : launch_decode_pair<false>(q, kv_cache, B, q_len, H, num_blocks, a, stream);
   if (st != MLA_OK) return st;
 
   const dim3 mgrid(static_cast<unsigned>(J) * (128 / mrg::kRows));
