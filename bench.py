@@ -331,11 +331,14 @@ def _roof(ms, bytes_, flops, hbm, tensor_tf, tensor_name):
             "frac": max(t_hbm, t_ten) / sec, "tensor_peak": tensor_name}
 
 
-def run_extras(device, flush, reps=10):
+def run_extras(device, flush, reps=10, only=None):
     """Every other workload of the path, timed on its own (each call after an
     L2 flush): the long single request, the fp8 KV cache, the speculative
     decode and its chunked-prefill context step, and the rotary embedding +
-    cache write of one decode step.  Inputs are seeded and synthetic."""
+    cache write of one decode step.  Inputs are seeded and synthetic.
+    `only` (long, fp8, spec, prefill or rope) runs just that one, e.g. for a
+    profiler."""
+    want = lambda name: only is None or only == name
     import mla_latent_kv_uk_gb300 as m
     import synth
     hbm, bf16, _ = peaks()
@@ -345,143 +348,149 @@ def run_extras(device, flush, reps=10):
     ex = {}
 
     # long single request: 131072 tokens as 8 explicit shards, merged
-    c3 = synth.config3()
-    S = 8
-    q3 = c3.q.to(device).expand(S, 1, 128, 576).contiguous()
-    bt3, sl3 = i32(np.repeat(c3.block_table, S, axis=0)), i32(np.repeat(c3.seq_lens, S))
-    st3 = i32([a for a, _ in c3.shards[0]])
-    en3 = i32([z for _, z in c3.shards[0]])
-    cache3 = c3.cache.to(device)
-    ws3 = torch.empty(m.mla_decode_workspace_size(S, 1, 128, bt3.shape[1] * 64),
-                      dtype=torch.uint8, device=device)
-    o3 = torch.empty((S, 1, 128, 512), dtype=torch.float32, device=device)
-    l3 = torch.empty((S, 1, 128), dtype=torch.float32, device=device)
+    if want("long"):
+        c3 = synth.config3()
+        S = 8
+        q3 = c3.q.to(device).expand(S, 1, 128, 576).contiguous()
+        bt3, sl3 = i32(np.repeat(c3.block_table, S, axis=0)), i32(np.repeat(c3.seq_lens, S))
+        st3 = i32([a for a, _ in c3.shards[0]])
+        en3 = i32([z for _, z in c3.shards[0]])
+        cache3 = c3.cache.to(device)
+        ws3 = torch.empty(m.mla_decode_workspace_size(S, 1, 128, bt3.shape[1] * 64),
+                          dtype=torch.uint8, device=device)
+        o3 = torch.empty((S, 1, 128, 512), dtype=torch.float32, device=device)
+        l3 = torch.empty((S, 1, 128), dtype=torch.float32, device=device)
 
-    def long_req():
-        m.mla_decode_paged(q3, cache3, bt3, sl3, sm_scale=c3.sm_scale, kv_starts=st3,
-                           kv_ends=en3, out_dtype=torch.float32, out=o3, lse=l3, workspace=ws3)
-        m.mla_merge_states(o3.view(S, 1, 128, 512), l3.view(S, 1, 128), out_dtype=torch.bfloat16)
-    n3 = int(c3.seq_lens.sum())
-    ex["long_b1_h128_ctx131072_8shards"] = dict(
-        _roof(_timed_call(long_req, flush, stream, reps),
-              n3 * 1152 + 128 * 576 * 2 + 128 * 512 * 2 + 128 * 4, 278528 * n3, hbm, bf16,
-              "bf16 measured"), calls="decode (8 shard rows) + merge_states")
-    del q3, cache3, ws3, o3, l3
+        def long_req():
+            m.mla_decode_paged(q3, cache3, bt3, sl3, sm_scale=c3.sm_scale, kv_starts=st3,
+                               kv_ends=en3, out_dtype=torch.float32, out=o3, lse=l3, workspace=ws3)
+            m.mla_merge_states(o3.view(S, 1, 128, 512), l3.view(S, 1, 128), out_dtype=torch.bfloat16)
+        n3 = int(c3.seq_lens.sum())
+        ex["long_b1_h128_ctx131072_8shards"] = dict(
+            _roof(_timed_call(long_req, flush, stream, reps),
+                  n3 * 1152 + 128 * 576 * 2 + 128 * 512 * 2 + 128 * 4, 278528 * n3, hbm, bf16,
+                  "bf16 measured"), calls="decode (8 shard rows) + merge_states")
+        del q3, cache3, ws3, o3, l3
 
     # fp8 KV cache: B = 64, ctx U[1024, 16384], e4m3 cache and query
-    c4 = synth.config4()
-    q4, cache4 = c4.q.to(device), c4.cache.to(device)
-    bt4, sl4 = i32(c4.block_table), i32(c4.seq_lens)
-    ws4 = torch.empty(m.mla_decode_workspace_size(c4.B, 1, 128, bt4.shape[1] * 64),
-                      dtype=torch.uint8, device=device)
-    o4 = torch.empty((c4.B, 1, 128, 512), dtype=torch.bfloat16, device=device)
-    l4 = torch.empty((c4.B, 1, 128), dtype=torch.float32, device=device)
-    n4 = int(c4.seq_lens.sum())
-    ms4 = _timed_call(lambda: m.mla_decode_paged(
-        q4, cache4, bt4, sl4, sm_scale=c4.sm_scale, q_scale=c4.q_scale, k_scale=c4.k_scale,
-        out=o4, lse=l4, workspace=ws4), flush, stream, reps)
-    ex["fp8_b64_h128_ctxU1k_16k"] = dict(
-        _roof(ms4, n4 * 576 + c4.B * 128 * (576 + 512 * 2 + 4), 278528 * n4, hbm, fp8_tf,
-              "fp8 = 2 x bf16 measured (nominal ratio)"),
-        tokens_per_s=c4.B / (ms4 * 1e-3), kv_tokens=n4)
-    del q4, cache4, ws4, o4, l4
+    if want("fp8"):
+        c4 = synth.config4()
+        q4, cache4 = c4.q.to(device), c4.cache.to(device)
+        bt4, sl4 = i32(c4.block_table), i32(c4.seq_lens)
+        ws4 = torch.empty(m.mla_decode_workspace_size(c4.B, 1, 128, bt4.shape[1] * 64),
+                          dtype=torch.uint8, device=device)
+        o4 = torch.empty((c4.B, 1, 128, 512), dtype=torch.bfloat16, device=device)
+        l4 = torch.empty((c4.B, 1, 128), dtype=torch.float32, device=device)
+        n4 = int(c4.seq_lens.sum())
+        ms4 = _timed_call(lambda: m.mla_decode_paged(
+            q4, cache4, bt4, sl4, sm_scale=c4.sm_scale, q_scale=c4.q_scale, k_scale=c4.k_scale,
+            out=o4, lse=l4, workspace=ws4), flush, stream, reps)
+        ex["fp8_b64_h128_ctxU1k_16k"] = dict(
+            _roof(ms4, n4 * 576 + c4.B * 128 * (576 + 512 * 2 + 4), 278528 * n4, hbm, fp8_tf,
+                  "fp8 = 2 x bf16 measured (nominal ratio)"),
+            tokens_per_s=c4.B / (ms4 * 1e-3), kv_tokens=n4)
+        del q4, cache4, ws4, o4, l4
 
     # speculative decode: B = 128, q_len 2 (causal pair), lognormal contexts
-    c5 = synth.config5_decode()
-    q5, cache5 = c5.q.to(device), c5.cache.to(device)
-    bt5, sl5 = i32(c5.block_table), i32(c5.seq_lens)
-    ws5 = torch.empty(m.mla_decode_workspace_size(c5.B, 2, 128, bt5.shape[1] * 64),
-                      dtype=torch.uint8, device=device)
-    o5 = torch.empty((c5.B, 2, 128, 512), dtype=torch.bfloat16, device=device)
-    l5 = torch.empty((c5.B, 2, 128), dtype=torch.float32, device=device)
-    n5 = int(c5.seq_lens.sum())
-    keys5 = int(2 * c5.seq_lens.sum() - c5.B)        # token 0 sees seq-1 keys, token 1 seq
-    ms5 = _timed_call(lambda: m.mla_decode_paged(q5, cache5, bt5, sl5, sm_scale=c5.sm_scale,
-                                                 out=o5, lse=l5, workspace=ws5),
-                      flush, stream, reps)
-    ex["spec_b128_q2_h128_lognormal"] = dict(
-        _roof(ms5, n5 * 1152 + c5.B * 2 * 128 * (576 * 2 + 512 * 2 + 4), 278528 * keys5,
-              hbm, bf16, "bf16 measured"),
-        tokens_per_s=c5.B * 2 / (ms5 * 1e-3), kv_tokens=n5,
-        note="each query token streams its request's latent rows (no sharing of a KV "
-             "tile between the two tokens): DRAM traffic is about twice the algorithmic bytes")
-    del q5, cache5, ws5, o5, l5
+    if want("spec"):
+        c5 = synth.config5_decode()
+        q5, cache5 = c5.q.to(device), c5.cache.to(device)
+        bt5, sl5 = i32(c5.block_table), i32(c5.seq_lens)
+        ws5 = torch.empty(m.mla_decode_workspace_size(c5.B, 2, 128, bt5.shape[1] * 64),
+                          dtype=torch.uint8, device=device)
+        o5 = torch.empty((c5.B, 2, 128, 512), dtype=torch.bfloat16, device=device)
+        l5 = torch.empty((c5.B, 2, 128), dtype=torch.float32, device=device)
+        n5 = int(c5.seq_lens.sum())
+        keys5 = int(2 * c5.seq_lens.sum() - c5.B)        # token 0 sees seq-1 keys, token 1 seq
+        ms5 = _timed_call(lambda: m.mla_decode_paged(q5, cache5, bt5, sl5, sm_scale=c5.sm_scale,
+                                                     out=o5, lse=l5, workspace=ws5),
+                          flush, stream, reps)
+        ex["spec_b128_q2_h128_lognormal"] = dict(
+            _roof(ms5, n5 * 1152 + c5.B * 2 * 128 * (576 * 2 + 512 * 2 + 4), 278528 * keys5,
+                  hbm, bf16, "bf16 measured"),
+            tokens_per_s=c5.B * 2 / (ms5 * 1e-3), kv_tokens=n5,
+            note="the two query tokens of a request are separate jobs; the planner orders "
+                 "jobs token-major so that their reads of a KV tile fall close together "
+                 "and the later one hits L2")
+        del q5, cache5, ws5, o5, l5
 
     # chunked-prefill context step: 4 x 8192 context rows on 4 interleaved
     # shards, 512 new tokens each, H = 128
-    cp = synth.config5_prefill()
-    smb = max(s_[1].shape[1] for s_ in cp.shards)
-    tables = []
-    for _, sbt, _ in cp.shards:
-        t_ = np.full((cp.B, smb), -1, np.int32)
-        t_[:, :sbt.shape[1]] = sbt
-        tables.append(i32(t_))
-    caches = [s_[0].to(device) for s_ in cp.shards]
-    cu_c = np.concatenate([[0], np.cumsum(cp.ctx_lens)]).astype(np.int32)
-    cu_q = np.concatenate([[0], np.cumsum(cp.new_lens)]).astype(np.int32)
-    dcu_c, dcu_q = i32(cu_c), i32(cu_q)
-    Nc, Tq, Hp = int(cu_c[-1]), int(cu_q[-1]), cp.H
-    rows = torch.empty((Nc, 576), dtype=torch.bfloat16, device=device)
-    w = cp.w_kvb.to(device)
-    kc = torch.empty((Nc, Hp, 192), dtype=torch.bfloat16, device=device)
-    vc = torch.empty((Nc, Hp, 128), dtype=torch.bfloat16, device=device)
-    new_kv = cp.new_kv.to(device)
-    qp = cp.q.to(device)
-    kn, vn = m.mla_expand_kv(new_kv, w, Hp)
-    mq = int(cp.new_lens.max())
-    oc = torch.empty((Tq, Hp, 128), dtype=torch.bfloat16, device=device)
-    lc = torch.empty((Tq, Hp), dtype=torch.float32, device=device)
-    on = torch.empty_like(oc)
-    ln = torch.empty_like(lc)
-    stages = {
-        "gather_reorg": (lambda: m.mla_gather_cache_reorg(caches, tables, dcu_c, Nc, interleave=1,
-                                                          out=rows),
-                         2 * Nc * 1152, 0),
-        "expand_context": (lambda: m.mla_expand_kv(rows, w, Hp, k_out=kc, v_out=vc),
-                           Nc * 1152 + Hp * 256 * 512 * 2 + Nc * Hp * 320 * 2,
-                           2 * Nc * 512 * Hp * 256),
-        "prefill_context": (lambda: m.mla_prefill_attn(qp, kc, vc, dcu_q, dcu_c, mq, causal=False,
-                                                       sm_scale=cp.sm_scale, out=oc, lse=lc),
-                            Tq * Hp * 192 * 2 + Nc * Hp * 320 * 2 + Tq * Hp * (128 * 2 + 4),
-                            2 * Hp * (192 + 128) * int(np.sum(cp.new_lens * cp.ctx_lens))),
-        "prefill_new_causal": (lambda: m.mla_prefill_attn(qp, kn, vn, dcu_q, dcu_q, mq,
-                                                          causal=True, sm_scale=cp.sm_scale,
-                                                          out=on, lse=ln),
-                               Tq * Hp * (192 + 192 + 128) * 2 + Tq * Hp * (128 * 2 + 4),
-                               2 * Hp * (192 + 128) * int(np.sum(cp.new_lens * (cp.new_lens + 1) // 2))),
-        "merge": (lambda: m.mla_merge_states(po, pl, out_dtype=torch.bfloat16, out=mo, out_lse=ml),
-                  Tq * Hp * (3 * 128 * 2 + 3 * 4), 0),
-    }
-    po = torch.empty((2, Tq, Hp, 128), dtype=torch.bfloat16, device=device)
-    pl = torch.empty((2, Tq, Hp), dtype=torch.float32, device=device)
-    mo = torch.empty((Tq, Hp, 128), dtype=torch.bfloat16, device=device)
-    ml = torch.empty((Tq, Hp), dtype=torch.float32, device=device)
-    ex_p = {}
-    for nm, (fn, b_, f_) in stages.items():
-        if nm == "merge":   # the two states, stacked outside the timed region
-            po[0].copy_(oc)
-            po[1].copy_(on)
-            pl[0].copy_(lc)
-            pl[1].copy_(ln)
-        fn()
-        ex_p[nm] = _roof(_timed_call(fn, flush, stream, reps), b_, f_, hbm, bf16, "bf16 measured")
-    ex["prefill_ctx_4x8192_w4_sq512_h128"] = ex_p
-    del caches, rows, kc, vc, kn, vn, oc, on, po, pl, mo, ml
+    if want("prefill"):
+        cp = synth.config5_prefill()
+        smb = max(s_[1].shape[1] for s_ in cp.shards)
+        tables = []
+        for _, sbt, _ in cp.shards:
+            t_ = np.full((cp.B, smb), -1, np.int32)
+            t_[:, :sbt.shape[1]] = sbt
+            tables.append(i32(t_))
+        caches = [s_[0].to(device) for s_ in cp.shards]
+        cu_c = np.concatenate([[0], np.cumsum(cp.ctx_lens)]).astype(np.int32)
+        cu_q = np.concatenate([[0], np.cumsum(cp.new_lens)]).astype(np.int32)
+        dcu_c, dcu_q = i32(cu_c), i32(cu_q)
+        Nc, Tq, Hp = int(cu_c[-1]), int(cu_q[-1]), cp.H
+        rows = torch.empty((Nc, 576), dtype=torch.bfloat16, device=device)
+        w = cp.w_kvb.to(device)
+        kc = torch.empty((Nc, Hp, 192), dtype=torch.bfloat16, device=device)
+        vc = torch.empty((Nc, Hp, 128), dtype=torch.bfloat16, device=device)
+        new_kv = cp.new_kv.to(device)
+        qp = cp.q.to(device)
+        kn, vn = m.mla_expand_kv(new_kv, w, Hp)
+        mq = int(cp.new_lens.max())
+        oc = torch.empty((Tq, Hp, 128), dtype=torch.bfloat16, device=device)
+        lc = torch.empty((Tq, Hp), dtype=torch.float32, device=device)
+        on = torch.empty_like(oc)
+        ln = torch.empty_like(lc)
+        stages = {
+            "gather_reorg": (lambda: m.mla_gather_cache_reorg(caches, tables, dcu_c, Nc, interleave=1,
+                                                              out=rows),
+                             2 * Nc * 1152, 0),
+            "expand_context": (lambda: m.mla_expand_kv(rows, w, Hp, k_out=kc, v_out=vc),
+                               Nc * 1152 + Hp * 256 * 512 * 2 + Nc * Hp * 320 * 2,
+                               2 * Nc * 512 * Hp * 256),
+            "prefill_context": (lambda: m.mla_prefill_attn(qp, kc, vc, dcu_q, dcu_c, mq, causal=False,
+                                                           sm_scale=cp.sm_scale, out=oc, lse=lc),
+                                Tq * Hp * 192 * 2 + Nc * Hp * 320 * 2 + Tq * Hp * (128 * 2 + 4),
+                                2 * Hp * (192 + 128) * int(np.sum(cp.new_lens * cp.ctx_lens))),
+            "prefill_new_causal": (lambda: m.mla_prefill_attn(qp, kn, vn, dcu_q, dcu_q, mq,
+                                                              causal=True, sm_scale=cp.sm_scale,
+                                                              out=on, lse=ln),
+                                   Tq * Hp * (192 + 192 + 128) * 2 + Tq * Hp * (128 * 2 + 4),
+                                   2 * Hp * (192 + 128) * int(np.sum(cp.new_lens * (cp.new_lens + 1) // 2))),
+            "merge": (lambda: m.mla_merge_states(po, pl, out_dtype=torch.bfloat16, out=mo, out_lse=ml),
+                      Tq * Hp * (3 * 128 * 2 + 3 * 4), 0),
+        }
+        po = torch.empty((2, Tq, Hp, 128), dtype=torch.bfloat16, device=device)
+        pl = torch.empty((2, Tq, Hp), dtype=torch.float32, device=device)
+        mo = torch.empty((Tq, Hp, 128), dtype=torch.bfloat16, device=device)
+        ml = torch.empty((Tq, Hp), dtype=torch.float32, device=device)
+        ex_p = {}
+        for nm, (fn, b_, f_) in stages.items():
+            if nm == "merge":   # the two states, stacked outside the timed region
+                po[0].copy_(oc)
+                po[1].copy_(on)
+                pl[0].copy_(lc)
+                pl[1].copy_(ln)
+            fn()
+            ex_p[nm] = _roof(_timed_call(fn, flush, stream, reps), b_, f_, hbm, bf16, "bf16 measured")
+        ex["prefill_ctx_4x8192_w4_sq512_h128"] = ex_p
+        del caches, rows, kc, vc, kn, vn, oc, on, po, pl, mo, ml
 
     # rotary embedding + cache write of one decode step at the DeepSeek-V3
     # shape (32 new tokens, 128 query heads)
-    g = synth.generator(9001)
-    T2 = 32
-    qpe = synth.as_bf16(g.standard_normal((T2, 128, 64))).to(device)
-    kpe = synth.as_bf16(g.standard_normal((T2, 64))).to(device)
-    kvc = synth.as_bf16(g.standard_normal((T2, 512))).to(device)
-    pos = i32(np.full(T2, 4095))
-    cache_r = torch.zeros((2048, 64, 576), dtype=torch.bfloat16, device=device)
-    slots = i32(np.arange(T2) * 64 + 63)
-    ms_r = _timed_call(lambda: m.mla_rope_cache_write(qpe, kpe, kvc, pos, slots, cache_r),
-                       flush, stream, reps)
-    ex["rope_cache_write_b32_h128"] = _roof(ms_r, T2 * (128 * 64 * 2 * 2 + 64 * 2 * 2 + 512 * 2 + 1152),
-                                            0, hbm, bf16, "-")
+    if want("rope"):
+        g = synth.generator(9001)
+        T2 = 32
+        qpe = synth.as_bf16(g.standard_normal((T2, 128, 64))).to(device)
+        kpe = synth.as_bf16(g.standard_normal((T2, 64))).to(device)
+        kvc = synth.as_bf16(g.standard_normal((T2, 512))).to(device)
+        pos = i32(np.full(T2, 4095))
+        cache_r = torch.zeros((2048, 64, 576), dtype=torch.bfloat16, device=device)
+        slots = i32(np.arange(T2) * 64 + 63)
+        ms_r = _timed_call(lambda: m.mla_rope_cache_write(qpe, kpe, kvc, pos, slots, cache_r),
+                           flush, stream, reps)
+        ex["rope_cache_write_b32_h128"] = _roof(ms_r, T2 * (128 * 64 * 2 * 2 + 64 * 2 * 2 + 512 * 2 + 1152),
+                                                0, hbm, bf16, "-")
     return ex
 
 
@@ -537,6 +546,9 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other workloads' timings (long request, fp8, spec decode, "
                          "prefill context step, rope + cache write)")
+    ap.add_argument("--only-extra", choices=["long", "fp8", "spec", "prefill", "rope"],
+                    help="time just that one of the other workloads and print its line "
+                         "(for a profiler); no main bench")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3) if args.impl == "ours" else args.warmup
 
@@ -551,6 +563,12 @@ def main():
 
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    if args.only_extra:
+        if rank == 0:
+            ex = run_extras(device, torch.empty(512 * 1024 * 1024, dtype=torch.uint8,
+                                                device=device), only=args.only_extra)
+            print(json.dumps({"extra": ex}), flush=True)
+        return
     if world > 1:
         torch.distributed.init_process_group("nccl", device_id=device)
     res = run_ours(args, rank, world, device)

@@ -192,7 +192,10 @@ int mla_decode_paged_noalloc(const void *q, int q_dtype, float q_scale,
                              int out_dtype, float *lse, mla_stream_t stream);
 
 /* A3 on its own: writes the split plan that mla_decode_paged computes.
- * Jobs are (b, i, head group of 128) in that nesting order; with the tile
+ * Jobs are (i, b, head group of 128) in that nesting order (query token
+ * outermost: with an even number of CTA pairs, the pairs working on the
+ * query tokens of a request then read the same key tiles at about the same
+ * time, so the later read finds them in L2); with the tile
  * size tk = 64 tokens (both kv dtypes; kv_dtype is kept so the tile may
  * differ by format), job j covers key tiles [lo/tk, ceil(hi/tk)); the jobs
  * are concatenated into one flat space where a non-empty job takes 4 units

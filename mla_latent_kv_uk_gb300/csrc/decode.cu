@@ -140,10 +140,10 @@ plan_kernel(const int32_t *__restrict__ seq_lens,
   int32_t *hi_a = lo_a + (J + 1);
   for (int j = threadIdx.x; j < J; j += blockDim.x) {
     const int bi = j / HG;
-    const int b = bi / q_len, i = bi % q_len;
+    const int i = bi / B, b = bi % B;   // token-major job order
     int len = seq_lens[b];
     if (len < 0 || len > max_blocks * kPage) {
-      if ((j % (q_len * HG)) == 0) raise_error(err, MLA_DEVERR_SEQ_LEN);
+      if (i == 0 && j % HG == 0) raise_error(err, MLA_DEVERR_SEQ_LEN);
       len = min(max(len, 0), max_blocks * kPage);
     }
     int hi = causal ? len - q_len + i + 1 : len;
@@ -210,10 +210,10 @@ plan_warp_kernel(const int32_t *__restrict__ seq_lens,
     t[k] = 0;
     if (k < per && j < J) {
       const int bi = j / HG;
-      const int b = bi / q_len, i = bi % q_len;
+      const int i = bi / B, b = bi % B;   // token-major job order
       int len = seq_lens[b];
       if (len < 0 || len > max_blocks * kPage) {
-        if ((j % (q_len * HG)) == 0) raise_error(err, MLA_DEVERR_SEQ_LEN);
+        if (i == 0 && j % HG == 0) raise_error(err, MLA_DEVERR_SEQ_LEN);
         len = min(max(len, 0), max_blocks * kPage);
       }
       int hi = causal ? len - q_len + i + 1 : len;
@@ -306,7 +306,7 @@ struct Seg {
 
 struct SegWalk {
   PlanView plan;
-  int q_len, H, HG, groups, tile;
+  int B, q_len, H, HG, groups, tile;
   int p, span_lo, span_hi, j;
   bool started;
 
@@ -314,6 +314,7 @@ struct SegWalk {
                        int g, int group_id, int tile_tokens) {
     plan = PlanView{pl, J};
     q_len = ql; H = h; HG = hg; groups = g; tile = tile_tokens;
+    B = J / (ql * hg);
     p = group_id;
     started = false;
   }
@@ -352,8 +353,9 @@ struct SegWalk {
         started = false;
         continue;
       }
+      // jobs are token-major: (query token i, request b, head group)
       const int bi = j / HG, hg = j % HG;
-      const int b = bi / q_len;
+      const int i = bi / B, b = bi % B;
       // independent loads, all in flight together
       const int t0 = tp[j], t1 = tp[j + 1];
       const int lo = plan.job_lo()[j], hi = plan.job_hi()[j];
@@ -370,7 +372,7 @@ struct SegWalk {
       if (u1 <= u0) { ++j; continue; }    // the span meets only the switch cost
       s.job = j;
       s.b = b;
-      s.row0 = bi * H + hg * 128;
+      s.row0 = (b * q_len + i) * H + hg * 128;
       s.out_row0 = s.row0;
       s.hrows = min(128, H - hg * 128);
       s.lo = lo;
@@ -1282,7 +1284,7 @@ struct Geo {
 
 template <typename Tout>
 __global__ void __launch_bounds__(256, 2)
-decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
+decode_merge_kernel(const int32_t *__restrict__ plan, int J, int q_len, int H, int HG,
                     const Tout *__restrict__ ws_o,
                     const float *__restrict__ ws_lse, Tout *out, float *lse, int *err) {
   using namespace mrg;
@@ -1373,7 +1375,9 @@ decode_merge_kernel(const int32_t *__restrict__ plan, int J, int H, int HG,
     }
   }
   if (hg * 128 + r >= H) return;
-  const int64_t orow = static_cast<int64_t>(j / HG) * H + hg * 128 + r;
+  // jobs are token-major: (query token i, request b, head group)
+  const int bq = J / (q_len * HG), i = (j / HG) / bq, b = (j / HG) % bq;
+  const int64_t orow = static_cast<int64_t>(b * q_len + i) * H + hg * 128 + r;
   const float inv = m == -INFINITY ? 0.f : 1.f / z;
   Tout *dst = out + orow * kLatent;
 #pragma unroll
@@ -1643,14 +1647,15 @@ extern "C" int mla_decode_paged(const void *q, int q_dtype, float q_scale,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
       e = launch_pdl(decode_merge_kernel<__nv_bfloat16>, mgrid, dim3(256), smem, stream, cplan, J,
-                     H, HG, reinterpret_cast<const __nv_bfloat16 *>(ws_o), cws_lse,
+                     q_len, H, HG, reinterpret_cast<const __nv_bfloat16 *>(ws_o), cws_lse,
                      static_cast<__nv_bfloat16 *>(out), lse, err);
   } else {
     constexpr int smem = mrg::Geo<float>::kSmem;
     e = cudaFuncSetAttribute(decode_merge_kernel<float>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess)
-      e = launch_pdl(decode_merge_kernel<float>, mgrid, dim3(256), smem, stream, cplan, J, H, HG,
+      e = launch_pdl(decode_merge_kernel<float>, mgrid, dim3(256), smem, stream, cplan, J, q_len,
+                     H, HG,
                      static_cast<const float *>(ws_o), cws_lse, static_cast<float *>(out), lse,
                      err);
   }

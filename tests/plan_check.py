@@ -34,12 +34,13 @@ TILE = 64   # key tokens per tile of the bf16 and e4m3 decode kernels
 
 
 def job_ranges(seq_lens, q_len, H, causal, kv_starts=None, kv_ends=None):
-    """Key range [lo, hi) of every job (request b, query token i, head group
-    of 128) in plan order, from the oracle's causal-range definition."""
+    """Key range [lo, hi) of every job (query token i, request b, head group
+    of 128: token-major, the documented plan order), from the oracle's
+    causal-range definition."""
     HG = (H + 127) // 128
     lo, hi = [], []
-    for b in range(len(seq_lens)):
-        for i in range(q_len):
+    for i in range(q_len):
+        for b in range(len(seq_lens)):
             a, z = O.decode_range(int(seq_lens[b]), q_len, i, causal,
                                   None if kv_starts is None else kv_starts[b],
                                   None if kv_ends is None else kv_ends[b])

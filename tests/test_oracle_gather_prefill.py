@@ -135,10 +135,11 @@ def test_plan_checker_rejects_corrupted_plans(field, idx, value):
 def test_job_ranges_follow_the_causal_definition():
     from tests.plan_check import job_ranges
     lo, hi = job_ranges([5, 0], 2, 200, True, kv_starts=[1, 0], kv_ends=[4, 9])
-    # request 0: token 0 sees keys < 4 -> [1,4); token 1 < 5 -> [1, min(5,4)=4)
-    # request 1: empty; two head groups per (request, token)
-    assert lo.tolist() == [1, 1, 1, 1, 0, 0, 0, 0]
-    assert hi.tolist() == [4, 4, 4, 4, 0, 0, 0, 0]
+    # token-major: (token 0: request 0, request 1), (token 1: request 0,
+    # request 1), two head groups each.  Request 0: token 0 sees keys < 4 ->
+    # [1,4); token 1 < 5 -> [1, min(5,4)=4).  Request 1: empty.
+    assert lo.tolist() == [1, 1, 0, 0, 1, 1, 0, 0]
+    assert hi.tolist() == [4, 4, 0, 0, 4, 4, 0, 0]
 
 
 def test_expand_brute_force():
