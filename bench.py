@@ -6,7 +6,10 @@ with shuffled physical blocks):
     mla_absorb_q (W_UK_T BMM + concat)  ->  mla_decode_paged (device split
     plan + tcgen05 paged decode + on-device merge)  ->  mla_v_up (W_UV).
 Inputs are synthetic (seeded), resident in HBM when the timed region starts.
-L2 is flushed (a 512 MiB write) before every timed step.
+L2 is flushed (a 512 MiB write) before every timed step.  The timed step is
+the three calls captured once into a CUDA graph and replayed; the eager
+launch of the same calls is reported beside it (`step_eager_ms`), and the
+end-to-end number (`e2e`) calls the API eagerly with host buffers.
 
 Prints ONE JSON line (rank 0).  --impl reference times the fp64 CPU oracle
 on a bounded sample of the same workload instead.
@@ -21,7 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
-import threading
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -64,21 +67,18 @@ class ClockSampler:
         q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
              "clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        # samples go to a file read after the timed region: a reader thread
+        # would take the GIL from the host thread while it enqueues a step
         try:
+            self.out = tempfile.TemporaryFile(mode="w+")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={q}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
+                stdout=self.out, stderr=subprocess.DEVNULL, text=True)
             time.sleep(0.3)
         except Exception:
             self.proc = None
         return self
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
 
     def __exit__(self, *a):
         if self.proc:
@@ -88,6 +88,9 @@ class ClockSampler:
                 self.proc.wait(timeout=5)
             except Exception:
                 self.proc.kill()
+            self.out.seek(0)
+            self.lines = [ln.strip() for ln in self.out.read().splitlines()]
+            self.out.close()
 
     def summary(self):
         sm, mx, reasons = [], None, set()
@@ -157,28 +160,27 @@ def run_ours(args, rank, world, device):
                            sm_scale=case.sm_scale, out=o_lat, lse=lse, workspace=ws)
         m.mla_v_up(o_lat.view(T, H, 512), d["w_uv"], out=y)
 
-    def timed(fn, k, has_dec=True):
-        """Per-step CUDA-event timing with an L2 flush before each step."""
-        tot, dec = [], []
+    def timed(fn, k):
+        """Per-step CUDA-event timing with an L2 flush before each step.  No
+        event sits between the calls of a step: an event record between two
+        kernels ends their programmatic-dependent-launch overlap."""
+        tot = []
         for _ in range(k):
             flush.zero_()
-            e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            fn(e1, e2)
-            e3.record(stream)
+            fn()
+            e1.record(stream)
             torch.cuda.synchronize()
-            tot.append(e0.elapsed_time(e3))
-            if has_dec:
-                dec.append(e1.elapsed_time(e2))
-        return tot, dec
+            tot.append(e0.elapsed_time(e1))
+        return tot
 
-    def device_step(e1, e2):
-        m.mla_absorb_q(d["q_nope"], d["q_pe"], d["w_uk_t"], out=q)
-        e1.record(stream)
+    def device_step():
+        step(d["q_nope"], d["q_pe"], d["bt"], d["sl"])
+
+    def decode_call():
         m.mla_decode_paged(q.view(B, 1, H, 576), d["cache"], d["bt"], d["sl"],
                            sm_scale=case.sm_scale, out=o_lat, lse=lse, workspace=ws)
-        e2.record(stream)
-        m.mla_v_up(o_lat.view(T, H, 512), d["w_uv"], out=y)
 
     def breakdown(k):
         """Per-call device times (ms) of the three entry points, each after an
@@ -203,48 +205,84 @@ def run_ours(args, rank, world, device):
             res[nm] = statistics.median(ts)
         return res
 
-    # host-buffer (end-to-end) variant: inputs copied from pinned host memory
-    # and the result read back every step, all inside the timed region
-    h_qn = d["q_nope"].cpu().pin_memory()
-    h_qp = d["q_pe"].cpu().pin_memory()
-    h_bt = d["bt"].cpu().pin_memory()
-    h_sl = d["sl"].cpu().pin_memory()
-    h_y = torch.empty(y.shape, dtype=y.dtype).pin_memory()
-    h_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    d_qn, d_qp = torch.empty_like(d["q_nope"]), torch.empty_like(d["q_pe"])
-    d_bt, d_sl = torch.empty_like(d["bt"]), torch.empty_like(d["sl"])
+    # host-buffer (end-to-end) variant: the step's inputs (q_nope, q_pe,
+    # block table, lengths) packed in one pinned host buffer and copied in
+    # with one copy, the result (v_up output + LSE, packed likewise) read
+    # back with one copy, all inside the timed region
+    def packed(tensors):
+        offs, n = [], 0
+        for t in tensors:
+            offs.append(n)
+            n += -(-t.numel() * t.element_size() // 256) * 256
+        return offs, n
 
-    def e2e_step(e1, e2):
-        d_qn.copy_(h_qn, non_blocking=True)
-        d_qp.copy_(h_qp, non_blocking=True)
-        d_bt.copy_(h_bt, non_blocking=True)
-        d_sl.copy_(h_sl, non_blocking=True)
-        step(d_qn, d_qp, d_bt, d_sl)
-        h_y.copy_(y, non_blocking=True)
-        h_lse.copy_(lse, non_blocking=True)
+    ins = (d["q_nope"], d["q_pe"], d["bt"], d["sl"])
+    in_offs, in_bytes = packed(ins)
+    h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(in_bytes, dtype=torch.uint8, device=device)
 
-    h2d = sum(t.numel() * t.element_size() for t in (h_qn, h_qp, h_bt, h_sl))
-    d2h = h_y.numel() * h_y.element_size() + h_lse.numel() * h_lse.element_size()
+    def view(buf, off, like):
+        nb = like.numel() * like.element_size()
+        return buf[off:off + nb].view(like.dtype).view(like.shape)
+
+    for t, o in zip(ins, in_offs):
+        view(h_in, o, t).copy_(t.cpu())
+    d_qn, d_qp, d_bt, d_sl = (view(d_in, o, t) for t, o in zip(ins, in_offs))
+    outs = (y, lse)
+    out_offs, out_bytes = packed(outs)
+    d_out = torch.empty(out_bytes, dtype=torch.uint8, device=device)
+    h_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    y_e, lse_e = (view(d_out, o, t) for t, o in zip(outs, out_offs))
+
+    def e2e_step():
+        d_in.copy_(h_in, non_blocking=True)
+        m.mla_absorb_q(d_qn, d_qp, d["w_uk_t"], out=q)
+        m.mla_decode_paged(q.view(B, 1, H, 576), d["cache"], d_bt, d_sl,
+                           sm_scale=case.sm_scale, out=o_lat, lse=lse_e, workspace=ws)
+        m.mla_v_up(o_lat.view(T, H, 512), d["w_uv"], out=y_e)
+        h_out.copy_(d_out, non_blocking=True)
+
+    h2d, d2h = in_bytes, out_bytes   # the two copies' sizes (256-byte padded parts)
 
     for _ in range(args.warmup):
-        device_step(torch.cuda.Event(), torch.cuda.Event())
-        e2e_step(None, None)
+        device_step()
+        e2e_step()
+    torch.cuda.synchronize()
+    # The timed step is the three calls captured once into a CUDA graph and
+    # replayed (the kernels, their arguments and their programmatic-launch
+    # edges are those of the eager calls; the host's launch work is gone).
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(2):
+            device_step()
+    torch.cuda.current_stream().wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        device_step()
+    for _ in range(args.warmup):
+        graph.replay()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
-        tot, dec = timed(device_step, args.steps)
+        tot = timed(graph.replay, args.steps)
+        # the same step with the three calls launched eagerly
+        eager = timed(device_step, args.steps)
+        # the decode call (plan + decode + merge) on its own, same flush, for
+        # its roofline
+        dec = timed(decode_call, args.steps)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    e2e_tot, _ = timed(e2e_step, args.steps, has_dec=False)
+    e2e_tot = timed(e2e_step, args.steps)
     parts = breakdown(max(3, min(args.steps, 10)))
     err = m.mla_get_device_error()
 
     ms, ms_e2e, ms_dec = max_over_ranks(
         [statistics.mean(tot), statistics.mean(e2e_tot),
-         statistics.mean(dec) if dec else float("nan")], world, device)
+         statistics.mean(dec)], world, device)
     bytes_, flops, kv_tokens = algorithmic_counts(case.seq_lens, B, H)
     hbm, bf16, src = peaks()
     achieved = bytes_ / (ms_dec * 1e-3) / 1e9
@@ -266,6 +304,7 @@ def run_ours(args, rank, world, device):
                      "kernel_ms": ms_dec, "peak_source": src,
                      "tensor_tflops": flops / (ms_dec * 1e-3) / 1e12,
                      "tensor_frac_of_bf16_peak": flops / (ms_dec * 1e-3) / 1e12 / bf16},
+        "step_eager_ms": max_over_ranks([statistics.mean(eager)], world, device)[0],
         "step_breakdown_ms": parts,
         "gpu_launches": 5 * args.steps,
         "clocks": clk.summary(),
