@@ -55,10 +55,11 @@ using namespace sm100;
 
 constexpr int kMinTiles = 4;                 // smallest auto span
 // Units of the flat split space a non-empty job takes on top of its tiles:
-// switching a CTA pair to a job costs its epilogue and query load, measured
-// at about four 64-token tiles, so a span that meets a job start is given
-// that many fewer tiles and spans that cross request boundaries end with
-// the others.
+// switching a CTA pair to a job costs its epilogue and query load (about
+// 2.5 us, two to three 64-token tiles), so a span that meets a job start is
+// given fewer tiles and spans that cross request boundaries end with the
+// others.  Four units timed best on the DeepSeek-V3 decode shape (B = 32,
+// 4096 tokens each) against two and three.
 constexpr int kJobCost = 4;
 constexpr float kRescaleLog2 = 8.f;          // lazy rescale threshold
 constexpr uint32_t kColO = 0, kColS = 256;   // TMEM columns (both variants)
@@ -302,6 +303,7 @@ struct Seg {
   int tile0, ntiles;    // first absolute tile, tiles in this segment
   int whole, slot;      // covers the whole job?  partial slot otherwise
   int len;              // seq_len of the request (set by the pair kernel's producer)
+  int qkc;              // ring index of the first of its two query stages (pair kernel)
 };
 
 struct SegWalk {
@@ -499,8 +501,14 @@ struct Fmt {
   static constexpr uint32_t kSboP = 8 * kPRow;
   static constexpr uint32_t kPMsg = 64 * kPRow + kAlMsg;   // bytes landing per P message
   static constexpr int kQCols = 64 * kEsz;                 // TMEM columns of the query half
+  // the query latent half enters through two ring stages, each holding two
+  // boxes of 64 columns x 128 rows in the latent swizzle
+  static constexpr int kQRow = 64 * kEsz;                  // bytes of a query box row
+  static constexpr int kQBox = 128 * kQRow;                // 16 / 8 KB
+  static constexpr int kQStageBytes = 2 * kQBox;
   static_assert(kStages <= kMaxStages && kStages * kStageBytes == 4 * 36864, "ring");
   static_assert(3 * kChunkSteps == kLatSteps + kRopeSteps, "three QK chunks");
+  static_assert(kQStageBytes <= kStageBytes && kQBox % 1024 == 0, "query stages");
 };
 }  // namespace pair
 
@@ -509,6 +517,7 @@ __global__ void __launch_bounds__(pair::kThreads, 1)
 decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
                    const __grid_constant__ CUtensorMap tm_kr,
                    const __grid_constant__ CUtensorMap tm_qr,
+                   const __grid_constant__ CUtensorMap tm_ql,
                    DecodeArgs args) {
   using namespace pair;
   using F = Fmt<FP8>;
@@ -621,6 +630,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       prefetch_tmap(&tm_kv);
       prefetch_tmap(&tm_kr);
       prefetch_tmap(&tm_qr);
+      prefetch_tmap(&tm_ql);
     }
     int kc = 0, nseg = 0;
     bool ok = true;
@@ -643,6 +653,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       return true;
     };
     while (ok && walk.next_warp(sg, args.seq_lens)) {
+      sg.qkc = kc;   // its query stages take the next two ring slots
       if (!(ok = publish(nseg, false))) break;
       const int32_t *bt = args.block_table + static_cast<int64_t>(sg.b) * args.max_blocks;
       int page_base = -(1 << 30), my_blk = -1;
@@ -681,16 +692,37 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
         ++kc;
         return true;
       };
-      // The first segment's query rope half goes out before any KV tile
-      // (nothing is in flight yet and QK(0) needs it).  A later segment
-      // loads its first KV tile, then its query rope half: the previous
-      // segment's last QK (which frees the rope buffer) completes about
-      // when the stage of this first tile frees up.
+      // Ring stage kc <- query latent columns [256*half + 128*i, +128) of
+      // the segment's 128 rows, as two boxes of 64 columns (the softmax
+      // warps move them into TMEM and the MMA thread frees the stage).
+      auto load_q_stage = [&](int i) -> bool {
+        const int s = kc % kStages;
+        if (kc >= kStages && !mbar_wait(&kv_empty[s], ((kc / kStages) - 1) & 1, abort_flag))
+          return false;
+        if (lane == 0) {
+          uint8_t *dst = sm_kv + s * kStageBytes;
+          mbar_arrive_expect_tx(&kv_full[s], F::kQStageBytes);
+          for (int j = 0; j < 2; ++j)
+            tma_load_2d(dst + j * F::kQBox, &tm_ql, &kv_full[s], 256 * half + 64 * (2 * i + j),
+                        sg.row0);
+        }
+        ++kc;
+        return true;
+      };
+      // The first segment's query rope half goes out before anything else
+      // (nothing is in flight yet and QK(0) needs it).  Every segment's
+      // query latent half comes next, ahead of its KV tiles: a later
+      // segment's is read into TMEM as soon as the previous segment's last
+      // QK is done.  A later segment then loads its first KV tile and its
+      // query rope half: the previous segment's last QK (which frees the
+      // rope buffer) completes about when the stage of this first tile
+      // frees up.
       const bool first = nseg == 0;
       if (first && lane == 0) {
         mbar_arrive_expect_tx(q_full, kQRopeBytes);
         tma_load_2d(sm_q, &tm_qr, q_full, kLatent + 32 * half, sg.row0);
       }
+      if (!(ok = load_q_stage(0) && load_q_stage(1))) break;
       const int pre = min(sg.ntiles, 1);
       for (int t = 0; ok && t < pre; ++t) ok = load_tile(sg.tile0 + t);
       if (!ok) break;
@@ -699,16 +731,6 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
         if (lane == 0) {
           mbar_arrive_expect_tx(q_full, kQRopeBytes);
           tma_load_2d(sm_q, &tm_qr, q_full, kLatent + 32 * half, sg.row0);
-          // The softmax warps read this segment's query rows at the end of
-          // the previous segment, about a ring's worth of tiles from now; a
-          // demand load then waits behind every SM's KV stream, so the
-          // rows (contiguous) are pulled into L2 here, in a few large
-          // prefetches (many small ones would hold up the TMA loads behind
-          // them).
-          const uint8_t *qrows = args.q + static_cast<int64_t>(sg.row0) * kDqk * F::kEsz;
-          const uint32_t bytes = static_cast<uint32_t>(sg.hrows) * kDqk * F::kEsz;
-          for (uint32_t o = 0; o < bytes; o += 16384)
-            prefetch_l2(qrows + o, min(16384u, bytes - o));
         }
       }
       ++nseg;
@@ -792,6 +814,11 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
         ok = mbar_wait(q_full, nseg & 1, abort_flag) &&
              mbar_wait(q_tmem, nseg & 1, abort_flag);
         if (!ok) break;
+        // the segment's two query stages are in TMEM: their ring slots go
+        // back to the producer, and its KV tiles follow them in the ring
+        mbar_arrive(&kv_empty[sg.qkc % kStages]);
+        mbar_arrive(&kv_empty[(sg.qkc + 1) % kStages]);
+        kc = sg.qkc + 2;
         ++nseg;
         // Fixed order, blocking waits: QK of the segment's first two tiles,
         // then for each tile t the QK of tile t+2 (the scores two tiles
@@ -900,24 +927,36 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
     auto warp_ok = [](bool v) { return __all_sync(0xffffffffu, v); };
     // Query latent dims [256*half, 256*half + 256) of row r -> TMEM columns
     // [kColQ, kColQ + F::kQCols): two bf16 or four e4m3 per 32-bit column.
-    auto load_q_tmem = [&](const Seg &seg) {
-      constexpr int kVec = F::kQCols / 4;   // 16-byte loads per row half
-      const uint4 *src = reinterpret_cast<const uint4 *>(
-                             args.q + static_cast<int64_t>(seg.row0 + r) * kDqk * F::kEsz) +
-                         kVec * half;
+    // The segment's query latent half: this thread's row out of the two
+    // ring stages (swizzled 16-byte chunks, conflict-free across a warp),
+    // then into TMEM; false on a timeout.
+    auto load_q_tmem = [&](const Seg &seg) -> bool {
+      constexpr int kCh = F::kQRow / 16;   // 16-byte chunks per box row
       const bool valid = r < seg.hrows;
-      // all loads in flight at once: under the KV stream every round trip
-      // to memory costs thousands of cycles
       uint32_t w[F::kQCols];
 #pragma unroll
-      for (int k = 0; k < kVec; ++k) {
-        uint4 v = valid ? __ldg(src + k) : make_uint4(0, 0, 0, 0);
-        w[4 * k] = v.x; w[4 * k + 1] = v.y; w[4 * k + 2] = v.z; w[4 * k + 3] = v.w;
+      for (int st = 0; st < 2; ++st) {
+        const int qs = seg.qkc + st;
+        if (!warp_ok(mbar_wait(&kv_full[qs % kStages], (qs / kStages) & 1, abort_flag)))
+          return false;
+        const uint8_t *stage = sm_kv + (qs % kStages) * kStageBytes;
+#pragma unroll
+        for (int bx = 0; bx < 2; ++bx) {
+          const uint4 *row = reinterpret_cast<const uint4 *>(stage + bx * F::kQBox + r * F::kQRow);
+#pragma unroll
+          for (int c = 0; c < kCh; ++c) {
+            uint4 v = row[FP8 ? (c ^ ((r >> 1) & 3)) : (c ^ (r & 7))];
+            if (!valid) v = make_uint4(0, 0, 0, 0);
+            const int k = 4 * ((2 * st + bx) * kCh + c);
+            w[k] = v.x; w[k + 1] = v.y; w[k + 2] = v.z; w[k + 3] = v.w;
+          }
+        }
       }
 #pragma unroll
       for (int c = 0; c < F::kQCols / 32; ++c) tmem_st_x32(lane_base + kColQ + 32 * c, w + 32 * c);
       tc_fence_before();
       mbar_arrive(q_tmem);
+      return true;
     };
     // Takes the next segment descriptor from the producer's queue
     // (warp-wide); false at the end marker or on a timeout (then ok = false).
@@ -935,7 +974,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
       return out.ntiles >= 0;
     };
     bool have = take_seg(sg);
-    if (have) load_q_tmem(sg);
+    if (have) ok = load_q_tmem(sg);
     Seg nxt;
     bool have_next = false;
     float l_in = 1.f;   // forwarded rows: the owner's running sum, last message
@@ -1131,7 +1170,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           const int nrows = kTile - first;
           // (every 16-byte chunk of a row: the swizzle only permutes them)
           constexpr int kCh = 4 * F::kEsz;   // 16-byte chunks per box row
-          uint8_t *vbase = sm_kv + (uc % kStages) * kStageBytes;
+          uint8_t *vbase = sm_kv + ((sg.qkc + 2 + t) % kStages) * kStageBytes;
           for (int idx = tid; idx < nrows * 4 * kCh; idx += 128) {
             const int box = idx / (nrows * kCh);
             const int rem = idx - box * nrows * kCh;
@@ -1148,7 +1187,7 @@ decode_pair_kernel(const __grid_constant__ CUtensorMap tm_kv,
           // TMEM now, overlapping the last P.V and the exchange with the peer
           have_next = take_seg(nxt);
           if (!ok) break;
-          if (have_next) load_q_tmem(nxt);
+          if (have_next && !(ok = load_q_tmem(nxt))) break;
         }
       }
       if (!ok) break;
@@ -1533,15 +1572,18 @@ int launch_decode_pair(const void *q, const void *kv_cache, int B, int q_len, in
   const uint32_t box_kv[2] = {64, static_cast<uint32_t>(pair::kTile)};
   const uint32_t box_kr[2] = {32, static_cast<uint32_t>(pair::kTile)};
   const uint32_t box_qr[2] = {32, 128};
+  const uint32_t box_ql[2] = {64, 128};
+  CUtensorMap tm_ql;
   if (!make_tmap(&tm_kv, dt, 2, kv_cache, kv_dims, strides, box_kv, sw_l) ||
       !make_tmap(&tm_kr, dt, 2, kv_cache, kv_dims, strides, box_kr, sw_r) ||
-      !make_tmap(&tm_qr, dt, 2, q, q_dims, strides, box_qr, sw_r))
+      !make_tmap(&tm_qr, dt, 2, q, q_dims, strides, box_qr, sw_r) ||
+      !make_tmap(&tm_ql, dt, 2, q, q_dims, strides, box_ql, sw_l))
     return MLA_ERR_CUDA;
   if (cudaFuncSetAttribute(decode_pair_kernel<FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            pair::kSmem) != cudaSuccess)
     return MLA_ERR_CUDA;
   PairLaunch pl(a.groups, stream);
-  if (cudaLaunchKernelEx(&pl.cfg, decode_pair_kernel<FP8>, tm_kv, tm_kr, tm_qr, a) !=
+  if (cudaLaunchKernelEx(&pl.cfg, decode_pair_kernel<FP8>, tm_kv, tm_kr, tm_qr, tm_ql, a) !=
       cudaSuccess)
     return MLA_ERR_CUDA;
   return MLA_OK;
