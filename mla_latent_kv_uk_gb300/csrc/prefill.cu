@@ -11,9 +11,13 @@
 //   S = Q K^T   tcgen05 M=128 N=128 K=192 (12 MMAs) into a TMEM buffer,
 //   P = exp2(S*scale*log2e - m) as bf16 written back over S in TMEM,
 //   O += P V    tcgen05 with A = P from TMEM, B = V (MN-major) from smem.
-// TMEM: S/P double buffer [0,256), O [256,384).  TMA fills a 2-stage ring
-// of K (48 KB) + V (32 KB) tiles.  Warp 0 = TMA, warp 1 = MMA, warps 2..5 =
-// softmax + epilogue (one query row per thread); lazy O rescaling.
+// TMEM: S/P double buffer [0,256), O [256,384).  K (48 KB) and V (32 KB)
+// tiles have rings of their own, two stages each: a K stage is refilled as
+// soon as the QK that read it is done, a tile and a half before P.V frees
+// the V stage of the same tile, so the next K tiles are in flight while the
+// softmax runs; the tiles a few steps further ahead are pulled into L2 by
+// tensor prefetches.  Warp 0 = TMA, warp 1 = MMA, warps 2..5 = softmax +
+// epilogue (one query row per thread); lazy O rescaling.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -25,15 +29,22 @@ namespace {
 
 using namespace sm100;
 
+// L2 prefetch of one tensor-map box (no shared memory, no completion).
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, int y, int z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+
 constexpr int kBM = 128, kBN = 128;
 constexpr int kDq = 192, kDv = 128;
 constexpr int kBox = 128 * 128;                  // 128 rows x 64 bf16
 constexpr int kQBytes = 3 * kBox;                // 48 KB
 constexpr int kKBytes = 3 * kBox;                // 48 KB
 constexpr int kVBytes = 2 * kBox;                // 32 KB
-constexpr int kStages = 2;
-constexpr int kStageBytes = kKBytes + kVBytes;
-constexpr int kSmemBytes = kQBytes + kStages * kStageBytes + 256 + 1024;
+constexpr int kStages = 2;                       // per ring (K and V)
+constexpr int kPrefetchAhead = 4;                // tiles pulled into L2 ahead
+constexpr int kSmemBytes = kQBytes + kStages * (kKBytes + kVBytes) + 256 + 1024;
 constexpr int kThreads = 192;
 constexpr uint32_t kColS = 0, kColO = 256;
 constexpr float kRescaleLog2 = 8.f;
@@ -70,10 +81,12 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sm_q = smem;
-  uint8_t *sm_kv = smem + kQBytes;
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_kv + kStages * kStageBytes);
-  uint64_t *kv_full = bars, *kv_empty = bars + kStages;
-  uint64_t *s_full = bars + 2 * kStages, *p_full = s_full + 2;
+  uint8_t *sm_k = smem + kQBytes;                      // [kStages] K tiles
+  uint8_t *sm_v = sm_k + kStages * kKBytes;            // [kStages] V tiles
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_v + kStages * kVBytes);
+  uint64_t *k_full = bars, *k_empty = bars + kStages;
+  uint64_t *v_full = bars + 2 * kStages, *v_empty = bars + 3 * kStages;
+  uint64_t *s_full = bars + 4 * kStages, *p_full = s_full + 2;
   uint64_t *pv_done = p_full + 2;             // [2], one per S/P buffer
   uint64_t *q_full = pv_done + 2, *drain = q_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
@@ -82,8 +95,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&kv_full[s], 1);
-      mbar_init(&kv_empty[s], 1);
+      mbar_init(&k_full[s], 1);
+      mbar_init(&k_empty[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&v_empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&s_full[s], 1);
@@ -116,21 +131,48 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       for (int d = 0; d < 3; ++d)
         tma_load_3d(sm_q + d * kBox, &tm_q, q_full, 64 * d, h, q0 + qt * kBM);
     }
-    for (; t < ntiles; ++t) {
-      const int s = t % kStages;
-      if (t >= kStages && !(ok = mbar_wait(&kv_empty[s], ((t / kStages) - 1) & 1, abort_flag)))
-        break;
-      uint8_t *dst = sm_kv + s * kStageBytes;
-      mbar_arrive_expect_tx(&kv_full[s], kStageBytes);
-      const int row = k0 + t * kBN;
-      for (int d = 0; d < 3; ++d) tma_load_3d(dst + d * kBox, &tm_k, &kv_full[s], 64 * d, h, row);
+    // K of tile t, then V of tile t - 1: K stages free up a tile and a
+    // half before the V stages of the same tiles
+    auto load_k = [&](int u) -> bool {
+      const int s = u % kStages;
+      if (u >= kStages && !mbar_wait(&k_empty[s], ((u / kStages) - 1) & 1, abort_flag))
+        return false;
+      mbar_arrive_expect_tx(&k_full[s], kKBytes);
+      const int row = k0 + u * kBN;
+      for (int d = 0; d < 3; ++d)
+        tma_load_3d(sm_k + s * kKBytes + d * kBox, &tm_k, &k_full[s], 64 * d, h, row);
+      // the tiles further ahead go to L2 now (the rings hold only two)
+      for (int a = (u == 0 ? kStages : kPrefetchAhead); a <= kPrefetchAhead; ++a) {
+        if (u + a < ntiles) {
+          const int prow = k0 + (u + a) * kBN;
+          for (int d = 0; d < 3; ++d) tma_prefetch_3d(&tm_k, 64 * d, h, prow);
+          for (int d = 0; d < 2; ++d) tma_prefetch_3d(&tm_v, 64 * d, h, prow);
+        }
+      }
+      return true;
+    };
+    auto load_v = [&](int u) -> bool {
+      const int s = u % kStages;
+      if (u >= kStages && !mbar_wait(&v_empty[s], ((u / kStages) - 1) & 1, abort_flag))
+        return false;
+      mbar_arrive_expect_tx(&v_full[s], kVBytes);
+      const int row = k0 + u * kBN;
       for (int d = 0; d < 2; ++d)
-        tma_load_3d(dst + kKBytes + d * kBox, &tm_v, &kv_full[s], 64 * d, h, row);
+        tma_load_3d(sm_v + s * kVBytes + d * kBox, &tm_v, &v_full[s], 64 * d, h, row);
+      return true;
+    };
+    int tv = 0;
+    for (; ok && t < ntiles; ++t) {
+      if (!(ok = load_k(t))) break;
+      if (t >= 1 && !(ok = load_v(tv++))) break;
     }
+    for (; ok && tv < ntiles; ++tv) ok = load_v(tv);
     if (*abort_flag) {
       volatile int no_abort = 0;
       for (int k = max(0, t - kStages); k < t; ++k)
-        mbar_wait(&kv_full[k % kStages], (k / kStages) & 1, &no_abort);
+        mbar_wait(&k_full[k % kStages], (k / kStages) & 1, &no_abort);
+      for (int k = max(0, tv - kStages); k < tv; ++k)
+        mbar_wait(&v_full[k % kStages], (k / kStages) & 1, &no_abort);
       if (ntiles > 0) mbar_wait(q_full, 0, &no_abort);
     }
   } else if (warp == 1 && lane == 0) {
@@ -139,7 +181,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     const uint32_t qa = smem_u32(sm_q);
     bool ok = ntiles == 0 || mbar_wait(q_full, 0, abort_flag);
     auto issue_qk = [&](int t) {
-      const uint32_t kb = smem_u32(sm_kv + (t % kStages) * kStageBytes);
+      const uint32_t kb = smem_u32(sm_k + (t % kStages) * kKBytes);
       const uint32_t d = tmem + kColS + 128 * (t & 1);
 #pragma unroll
       for (int k = 0; k < kDq / 16; ++k)
@@ -147,9 +189,10 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                    sdesc(kb + (k >> 2) * kBox + (k & 3) * 32, 16, 1024, kSwizzle128B),
                    idesc_qk, k > 0);
       mma_commit(&s_full[t & 1]);
+      mma_commit(&k_empty[t % kStages]);   // the K stage is read
     };
     if (ok && ntiles > 0) {
-      ok = mbar_wait(&kv_full[0], 0, abort_flag);
+      ok = mbar_wait(&k_full[0], 0, abort_flag);
       if (ok) {
         tc_fence_after();
         issue_qk(0);
@@ -157,20 +200,22 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
     }
     for (int t = 0; ok && t < ntiles; ++t) {
       if (t + 1 < ntiles) {
-        if (!(ok = mbar_wait(&kv_full[(t + 1) % kStages], ((t + 1) / kStages) & 1, abort_flag)))
+        if (!(ok = mbar_wait(&k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1, abort_flag)))
           break;
         tc_fence_after();
         issue_qk(t + 1);
       }
-      if (!(ok = mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag))) break;
+      if (!(ok = mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag) &&
+                 mbar_wait(&v_full[t % kStages], (t / kStages) & 1, abort_flag)))
+        break;
       tc_fence_after();
-      const uint32_t vb = smem_u32(sm_kv + (t % kStages) * kStageBytes + kKBytes);
+      const uint32_t vb = smem_u32(sm_v + (t % kStages) * kVBytes);
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk)
         mma_f16_ts(tmem + kColO, tmem + kColS + 128 * (t & 1) + 8 * kk,
                    sdesc(vb + kk * 2048, kBox, 1024, kSwizzle128B), idesc_pv,
                    (t > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(&kv_empty[t % kStages]);
+      mma_commit(&v_empty[t % kStages]);
       mma_commit(&pv_done[t & 1]);
     }
     if (!ok) {
