@@ -235,19 +235,25 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       const int sb = t & 1;
       if (!(ok = mbar_wait(&s_full[sb], (t >> 1) & 1, abort_flag))) break;
       tc_fence_after();
+      // raw scores; only a tile that crosses this row's limit is masked
       float x[kBN];
-      float tmax = -INFINITY;
 #pragma unroll
       for (int c = 0; c < kBN; c += 32) {
         uint32_t v[32];
         tmem_ld_x32(lane_base + kColS + 128 * sb + c, v);
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const int j = t * kBN + c + k;
-          x[c + k] = j < lim ? __uint_as_float(v[k]) * args.scale_log2 : -INFINITY;
-          tmax = fmaxf(tmax, x[c + k]);
-        }
+        for (int k = 0; k < 32; ++k) x[c + k] = __uint_as_float(v[k]);
       }
+      if ((t + 1) * kBN > lim) {
+#pragma unroll
+        for (int k = 0; k < kBN; ++k) x[k] = t * kBN + k < lim ? x[k] : -INFINITY;
+      }
+      // tile max on the raw scores (four chains), scaled once: scaling by a
+      // positive constant keeps the order and rounds each value alike
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+      for (int k = 0; k < kBN; k += 2) mx[(k >> 1) & 3] = fmax3(mx[(k >> 1) & 3], x[k], x[k + 1]);
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * args.scale_log2;
       if (t > 0) {
         const float m_new = fmaxf(m, tmax);
         const bool need = m_new > m + kRescaleLog2 || (m == -INFINITY && m_new > -INFINITY);
@@ -273,17 +279,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         m = tmax;
       }
       const float ms = m == -INFINITY ? 0.f : m;
-      // row sum of the unrounded probabilities (see the decode kernel)
-      float psum = 0.f;
+      // p = 2^(s * scale - m): paired FMAs, then the hardware ex2; the row
+      // sum of the unrounded probabilities (see the decode kernel) in four
+      // chains of paired adds
+      const float nm = -ms, sc = args.scale_log2;
+#pragma unroll
+      for (int k = 0; k < kBN; k += 2) fma_f32x2(x[k], x[k + 1], x[k], x[k + 1], sc, sc, nm, nm);
+#pragma unroll
+      for (int k = 0; k < kBN; ++k) x[k] = ex2(x[k]);
+      float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int k = 0; k < kBN; k += 4) {
+        add_f32x2(ps[0], ps[1], ps[0], ps[1], x[k], x[k + 1]);
+        add_f32x2(ps[2], ps[3], ps[2], ps[3], x[k + 2], x[k + 3]);
+      }
+      const float psum = (ps[0] + ps[1]) + (ps[2] + ps[3]);
 #pragma unroll
       for (int c = 0; c < kBN; c += 64) {
         uint32_t pk[32];
 #pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          const float p0 = ex2(x[c + 2 * k] - ms), p1 = ex2(x[c + 2 * k + 1] - ms);
-          psum += p0 + p1;
-          pk[k] = pack2(p0, p1);
-        }
+        for (int k = 0; k < 32; ++k) pk[k] = pack2(x[c + 2 * k], x[c + 2 * k + 1]);
         tmem_st_x32(lane_base + kColS + 128 * sb + c / 2, pk);
       }
       l += psum;
