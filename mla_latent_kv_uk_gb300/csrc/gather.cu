@@ -1,9 +1,12 @@
 // A7: paged gather (plain bit copy or e4m3 -> bf16 dequantisation) and the
 // fused gather + interleaved-shard reorg.
 //
-// Both are HBM-bound copies: one warp moves one 576-element row with
-// 16-byte vector accesses, so every request row is read once and written
-// once (1152 B + 1152 B for bf16).  Sources:
+// Both are HBM-bound copies: every request row is read once and written
+// once (1152 B + 1152 B for bf16).  A warp takes eight consecutive output
+// rows: lanes 0..7 find the eight source rows at once (the segment search
+// and block-table reads are dependent loads, so doing them per row would
+// leave the copy waiting on them), then all 32 lanes move the eight rows
+// with every 16-byte load in flight before the first store.  Sources:
 //   "DeepSeek MLA 在 DCP 分布式环境中的 Prefill 阶段解析", §与非 DCP 的流程对比
 //   (local gather, rank-major all-gather, reorg_kvcache) and §关于
 //   cp_gather_cache 的命名澄清 (gather without dequantisation);
@@ -33,40 +36,57 @@ __device__ __forceinline__ int find_segment(const int32_t *cu, int n, int row) {
   return lo;
 }
 
-// Copies (or dequantises) one 576-element row; `src == nullptr` zeroes it.
-template <int MODE>
-__device__ __forceinline__ void copy_row(const uint8_t *src, uint8_t *dst,
-                                         float k_scale, int lane) {
-  if (MODE == kCopyBf16 || MODE == kCopyE4m3) {
-    constexpr int chunks = MODE == kCopyBf16 ? kDqk * 2 / 16 : kDqk / 16;
-    const uint4 *s = reinterpret_cast<const uint4 *>(src);
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-    for (int c = lane; c < chunks; c += 32)
-      d[c] = src ? __ldcs(s + c) : make_uint4(0, 0, 0, 0);
-  } else {
-    // 72 chunks of 8 e4m3 codes -> 8 bf16 (16 bytes) each
-    const uint2 *s = reinterpret_cast<const uint2 *>(src);
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-    for (int c = lane; c < kDqk / 8; c += 32) {
-      if (!src) { d[c] = make_uint4(0, 0, 0, 0); continue; }
-      uint2 v = __ldcs(s + c);
-      uint32_t w[2] = {v.x, v.y};
-      uint32_t o[4];
+constexpr int kRowsPerWarp = 8;
+
+// Eight e4m3 codes -> eight bf16: exact e4m3 -> f16 -> f32, one fp32
+// multiply by k_scale, one RNE rounding to bf16.
+__device__ __forceinline__ uint4 dequant8(uint2 v, float k_scale) {
+  const uint32_t w[2] = {v.x, v.y};
+  uint32_t o[4];
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        // two codes per step: exact e4m3 -> f16 -> f32, one fp32 multiply,
-        // one RNE rounding to bf16
-        __nv_fp8x2_storage_t pair =
-            static_cast<__nv_fp8x2_storage_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
-        __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-        float2 f = __half22float2(*reinterpret_cast<__half2 *>(&h));
-        __nv_bfloat16 lo = __float2bfloat16_rn(__fmul_rn(f.x, k_scale));
-        __nv_bfloat16 hi = __float2bfloat16_rn(__fmul_rn(f.y, k_scale));
-        o[k] = static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
-               (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
-      }
-      d[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  for (int k = 0; k < 4; ++k) {
+    __nv_fp8x2_storage_t pair =
+        static_cast<__nv_fp8x2_storage_t>((w[k >> 1] >> ((k & 1) * 16)) & 0xFFFFu);
+    __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+    float2 f = __half22float2(*reinterpret_cast<__half2 *>(&h));
+    __nv_bfloat16 lo = __float2bfloat16_rn(__fmul_rn(f.x, k_scale));
+    __nv_bfloat16 hi = __float2bfloat16_rn(__fmul_rn(f.y, k_scale));
+    o[k] = static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
+           (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Copies (or dequantises) the warp's eight 576-element rows.  Lane i < 8
+// holds row i's source (nullptr: the row is zeroed) and destination
+// (nullptr: the row is not written).  Lanes take consecutive 16-byte output
+// chunks, so every load and store instruction covers whole rows' runs.
+template <int MODE>
+__device__ __forceinline__ void copy_rows(const uint8_t *src_lane, uint8_t *dst_lane,
+                                          float k_scale, int lane) {
+  constexpr int C = MODE == kCopyE4m3 ? kDqk / 16 : kDqk * 2 / 16;   // output chunks per row
+  constexpr int N = kRowsPerWarp * C / 32;                            // per lane: 9 or 18
+  static_assert(kRowsPerWarp * C % 32 == 0, "whole chunks per lane");
+  const unsigned long long s64 = reinterpret_cast<unsigned long long>(src_lane);
+  const unsigned long long d64 = reinterpret_cast<unsigned long long>(dst_lane);
+  uint4 v[N];
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const int idx = lane + 32 * i, row = idx / C, c = idx - row * C;
+    const uint8_t *src = reinterpret_cast<const uint8_t *>(__shfl_sync(0xffffffffu, s64, row));
+    if (!src) {
+      v[i] = make_uint4(0, 0, 0, 0);
+    } else if (MODE == kDequant) {
+      v[i] = dequant8(__ldcs(reinterpret_cast<const uint2 *>(src) + c), k_scale);
+    } else {
+      v[i] = __ldcs(reinterpret_cast<const uint4 *>(src) + c);
     }
+  }
+#pragma unroll
+  for (int i = 0; i < N; ++i) {
+    const int idx = lane + 32 * i, row = idx / C, c = idx - row * C;
+    uint8_t *dst = reinterpret_cast<uint8_t *>(__shfl_sync(0xffffffffu, d64, row));
+    if (dst) reinterpret_cast<uint4 *>(dst)[c] = v[i];
   }
 }
 
@@ -80,25 +100,27 @@ gather_kernel(const uint8_t *__restrict__ cache, int in_row_bytes,
               int num_blocks, int total_rows, float k_scale, uint8_t *out,
               int out_row_bytes, int *err) {
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (row >= total_rows) return;
-  if (row < __ldg(cu_out) || row >= __ldg(cu_out + B)) return;
-  const int b = find_segment(cu_out, B, row);
-  const int j = row - __ldg(cu_out + b);
-  const int pos = (seq_starts ? __ldg(seq_starts + b) : 0) + j;
-  const int len = __ldg(seq_lens + b);
+  const int row0 = (blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * kRowsPerWarp;
+  if (row0 >= total_rows) return;   // uniform across the warp
   const uint8_t *src = nullptr;
-  if (pos < 0 || pos >= len || pos / kPage >= max_blocks) {
-    if (lane == 0) raise_error(err, MLA_DEVERR_RANGE);
-  } else {
-    const int blk = __ldg(block_table + static_cast<int64_t>(b) * max_blocks + pos / kPage);
-    if (blk < 0 || blk >= num_blocks) {
-      if (lane == 0) raise_error(err, MLA_DEVERR_BLOCK_ID);
+  uint8_t *dst = nullptr;
+  const int row = row0 + lane;
+  if (lane < kRowsPerWarp && row < total_rows && row >= __ldg(cu_out) &&
+      row < __ldg(cu_out + B)) {
+    dst = out + static_cast<int64_t>(row) * out_row_bytes;
+    const int b = find_segment(cu_out, B, row);
+    const int j = row - __ldg(cu_out + b);
+    const int pos = (seq_starts ? __ldg(seq_starts + b) : 0) + j;
+    const int len = __ldg(seq_lens + b);
+    if (pos < 0 || pos >= len || pos / kPage >= max_blocks) {
+      raise_error(err, MLA_DEVERR_RANGE);
     } else {
-      src = cache + (static_cast<int64_t>(blk) * kPage + pos % kPage) * in_row_bytes;
+      const int blk = __ldg(block_table + static_cast<int64_t>(b) * max_blocks + pos / kPage);
+      if (blk < 0 || blk >= num_blocks) raise_error(err, MLA_DEVERR_BLOCK_ID);
+      else src = cache + (static_cast<int64_t>(blk) * kPage + pos % kPage) * in_row_bytes;
     }
   }
-  copy_row<MODE>(src, out + static_cast<int64_t>(row) * out_row_bytes, k_scale, lane);
+  copy_rows<MODE>(src, dst, k_scale, lane);
 }
 
 struct ShardSet {
@@ -115,15 +137,14 @@ __device__ __forceinline__ void shard_of(int t, int W, int I, int &k, int &j) {
 
 __device__ __forceinline__ const uint8_t *shard_row(const ShardSet &s, int k,
                                                     int r, int j, int smb,
-                                                    int row_bytes, int *err,
-                                                    int lane) {
+                                                    int row_bytes, int *err) {
   if (j / kPage >= smb) {
-    if (lane == 0) raise_error(err, MLA_DEVERR_RANGE);
+    raise_error(err, MLA_DEVERR_RANGE);
     return nullptr;
   }
   const int blk = __ldg(s.table[k] + static_cast<int64_t>(r) * smb + j / kPage);
   if (blk < 0 || blk >= s.num_blocks[k]) {
-    if (lane == 0) raise_error(err, MLA_DEVERR_BLOCK_ID);
+    raise_error(err, MLA_DEVERR_BLOCK_ID);
     return nullptr;
   }
   return s.cache[k] + (static_cast<int64_t>(blk) * kPage + j % kPage) * row_bytes;
@@ -136,15 +157,21 @@ reorg_kernel(ShardSet shards, int W, int I, int smb, int in_row_bytes,
              const int32_t *__restrict__ cu_out, int B, int total_rows,
              float k_scale, uint8_t *out, int out_row_bytes, int *err) {
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (row >= total_rows) return;
-  if (row < __ldg(cu_out) || row >= __ldg(cu_out + B)) return;
-  const int r = find_segment(cu_out, B, row);
-  const int t = row - __ldg(cu_out + r);
-  int k, j;
-  shard_of(t, W, I, k, j);
-  const uint8_t *src = shard_row(shards, k, r, j, smb, in_row_bytes, err, lane);
-  copy_row<MODE>(src, out + static_cast<int64_t>(row) * out_row_bytes, k_scale, lane);
+  const int row0 = (blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * kRowsPerWarp;
+  if (row0 >= total_rows) return;   // uniform across the warp
+  const uint8_t *src = nullptr;
+  uint8_t *dst = nullptr;
+  const int row = row0 + lane;
+  if (lane < kRowsPerWarp && row < total_rows && row >= __ldg(cu_out) &&
+      row < __ldg(cu_out + B)) {
+    dst = out + static_cast<int64_t>(row) * out_row_bytes;
+    const int r = find_segment(cu_out, B, row);
+    const int t = row - __ldg(cu_out + r);
+    int k, j;
+    shard_of(t, W, I, k, j);
+    src = shard_row(shards, k, r, j, smb, in_row_bytes, err);
+  }
+  copy_rows<MODE>(src, dst, k_scale, lane);
 }
 
 // Rank-major all-gather buffer: row k*sum_p + padded_cu[r] + j.
@@ -155,24 +182,26 @@ rank_major_kernel(ShardSet shards, int W, int I, int smb, int in_row_bytes,
                   const int32_t *__restrict__ padded_cu, int B, int sum_p,
                   float k_scale, uint8_t *out, int out_row_bytes, int *err) {
   const int lane = threadIdx.x & 31;
-  const int row = blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5);
-  if (row >= W * sum_p) return;
-  const int k = row / sum_p;
-  const int rem = row - k * sum_p;
-  uint8_t *dst = out + static_cast<int64_t>(row) * out_row_bytes;
-  if (rem >= __ldg(padded_cu + B)) {
-    copy_row<MODE>(nullptr, dst, k_scale, lane);
-    return;
-  }
-  const int r = find_segment(padded_cu, B, rem);
-  const int j = rem - __ldg(padded_cu + r);
-  const int ctx = __ldg(cu_out + r + 1) - __ldg(cu_out + r);
-  const int cyc = I * W;
-  const int rm = ctx % cyc;
-  const int n_k = (ctx / cyc) * I + min(max(rm - k * I, 0), I);
+  const int row0 = (blockIdx.x * kWarpsPerBlock + (threadIdx.x >> 5)) * kRowsPerWarp;
+  if (row0 >= W * sum_p) return;   // uniform across the warp
   const uint8_t *src = nullptr;
-  if (j < n_k) src = shard_row(shards, k, r, j, smb, in_row_bytes, err, lane);
-  copy_row<MODE>(src, dst, k_scale, lane);
+  uint8_t *dst = nullptr;
+  const int row = row0 + lane;
+  if (lane < kRowsPerWarp && row < W * sum_p) {
+    const int k = row / sum_p;
+    const int rem = row - k * sum_p;
+    dst = out + static_cast<int64_t>(row) * out_row_bytes;
+    if (rem < __ldg(padded_cu + B)) {   // else a padding row: zeros
+      const int r = find_segment(padded_cu, B, rem);
+      const int j = rem - __ldg(padded_cu + r);
+      const int ctx = __ldg(cu_out + r + 1) - __ldg(cu_out + r);
+      const int cyc = I * W;
+      const int rm = ctx % cyc;
+      const int n_k = (ctx / cyc) * I + min(max(rm - k * I, 0), I);
+      if (j < n_k) src = shard_row(shards, k, r, j, smb, in_row_bytes, err);
+    }
+  }
+  copy_rows<MODE>(src, dst, k_scale, lane);
 }
 
 int mode_of(int kv_dtype, int out_dtype) {
@@ -207,7 +236,8 @@ extern "C" int mla_gather_cache(const void *kv_cache, int kv_dtype,
   if (!err) return MLA_ERR_CUDA;
   const int in_bytes = kv_dtype == MLA_BF16 ? kDqk * 2 : kDqk;
   const int out_bytes = out_dtype == MLA_BF16 ? kDqk * 2 : kDqk;
-  dim3 grid((total_rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+  constexpr int kRowsPerBlock = kWarpsPerBlock * kRowsPerWarp;
+  dim3 grid((total_rows + kRowsPerBlock - 1) / kRowsPerBlock);
   auto *src = static_cast<const uint8_t *>(kv_cache);
   auto *dst = static_cast<uint8_t *>(out);
 #define MLA_GATHER(M)                                                        \
@@ -253,8 +283,9 @@ extern "C" int mla_gather_cache_reorg(
   const int in_bytes = kv_dtype == MLA_BF16 ? kDqk * 2 : kDqk;
   const int out_bytes = out_dtype == MLA_BF16 ? kDqk * 2 : kDqk;
   auto *dst = static_cast<uint8_t *>(out);
+  constexpr int kRowsPerBlock = kWarpsPerBlock * kRowsPerWarp;
   if (total_rows > 0) {
-    dim3 grid((total_rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    dim3 grid((total_rows + kRowsPerBlock - 1) / kRowsPerBlock);
 #define MLA_REORG(M)                                                         \
   reorg_kernel<M><<<grid, kWarpsPerBlock * 32, 0, stream>>>(                 \
       s, W, interleave, shard_max_blocks, in_bytes, cu_out, B, total_rows,   \
@@ -268,7 +299,7 @@ extern "C" int mla_gather_cache_reorg(
   if (rank_major_out && rank_major_rows > 0) {
     const int sum_p = rank_major_rows / W;
     auto *rm = static_cast<uint8_t *>(rank_major_out);
-    dim3 grid((rank_major_rows + kWarpsPerBlock - 1) / kWarpsPerBlock);
+    dim3 grid((rank_major_rows + kRowsPerBlock - 1) / kRowsPerBlock);
 #define MLA_RANKMAJOR(M)                                                     \
   rank_major_kernel<M><<<grid, kWarpsPerBlock * 32, 0, stream>>>(            \
       s, W, interleave, shard_max_blocks, in_bytes, cu_out, padded_cu, B,    \
