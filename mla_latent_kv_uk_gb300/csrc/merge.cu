@@ -5,8 +5,8 @@
 // combines per-rank partials by LSE weighting).
 //
 // HBM-bound: every partial row is read once with 16-byte loads and the
-// merged row written once; one thread per 16-byte chunk for a few parts of
-// short rows, one warp per (t, h) row otherwise.
+// merged row written once; one thread per 16-byte chunk for up to eight
+// parts, one warp per (t, h) row otherwise.
 #include <cuda_bf16.h>
 
 #include "common.cuh"
@@ -29,13 +29,13 @@ merge_kernel(const Tin *__restrict__ parts, const float *__restrict__ plse,
                        out_lse ? out_lse + row : nullptr, threadIdx.x & 31);
 }
 
-// Few parts (S <= 4, the usual shard or prefix / suffix merge) of rows of
-// at most 256 values: one thread per 16-byte chunk of the output (8
-// values), every thread reading its row's S LSEs itself, so no shuffles and
-// every SM full of independent loads.  A part of weight 0 is never read.
+// Few parts (S <= SMAX: 4, the usual shard or prefix / suffix merge, or 8):
+// one thread per 16-byte chunk of the output (8 values), every thread
+// reading its row's S LSEs itself, so no shuffles and every SM full of
+// independent loads.  A part of weight 0 is never read.
 constexpr int kChunkThreads = 256;
 
-template <typename Tin, typename Tout>
+template <typename Tin, typename Tout, int SMAX>
 __global__ void __launch_bounds__(kChunkThreads)
 merge_chunks_kernel(const Tin *__restrict__ parts, const float *__restrict__ plse, int S,
                     int64_t rows, int cpr, Tout *out, float *out_lse) {
@@ -44,9 +44,9 @@ merge_chunks_kernel(const Tin *__restrict__ parts, const float *__restrict__ pls
   const int c = static_cast<int>(g - row * cpr);
   if (row >= rows) return;
   const int D = cpr * 8;
-  float l[4], m = -INFINITY;
+  float l[SMAX], m = -INFINITY;
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = 0; s < SMAX; ++s) {
     l[s] = s < S ? plse[s * rows + row] : -INFINITY;
     m = fmaxf(m, l[s]);
   }
@@ -57,19 +57,19 @@ merge_chunks_kernel(const Tin *__restrict__ parts, const float *__restrict__ pls
     if (out_lse && c == 0) out_lse[row] = -INFINITY;
     return;
   }
-  float w[4], z = 0.f;
+  float w[SMAX], z = 0.f;
 #pragma unroll
-  for (int s = 0; s < 4; ++s) {
+  for (int s = 0; s < SMAX; ++s) {
     w[s] = l[s] == -INFINITY ? 0.f : expf(l[s] - m);
     z += w[s];
   }
-  float v[4][8];
+  float v[SMAX][8];
 #pragma unroll
-  for (int s = 0; s < 4; ++s)
+  for (int s = 0; s < SMAX; ++s)
     if (w[s] != 0.f) load8(parts + (s * rows + row) * D + c * 8, v[s]);
   float acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
 #pragma unroll
-  for (int s = 0; s < 4; ++s)
+  for (int s = 0; s < SMAX; ++s)
     if (w[s] != 0.f) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) acc[e] = fmaf(w[s], v[s][e], acc[e]);
@@ -101,13 +101,21 @@ extern "C" int mla_merge_states(const void *parts_out, int parts_dtype,
   const int64_t rows64 = static_cast<int64_t>(T) * H;
   if (rows64 > (1ll << 30)) return MLA_ERR_INVALID_ARG;
   const int rows = static_cast<int>(rows64);
-  if (S <= 4 && D <= 256) {
+  if (S <= 8) {
+    // S <= 4 takes the 4-slot form (fewer registers), 5..8 the 8-slot one
     const int cpr = D / 8;
     const dim3 cgrid(static_cast<unsigned>((rows64 * cpr + kChunkThreads - 1) / kChunkThreads));
 #define MLA_MERGE_C(TI, TO)                                                   \
-  merge_chunks_kernel<TI, TO><<<cgrid, kChunkThreads, 0, stream>>>(          \
-      static_cast<const TI *>(parts_out), parts_lse, S, rows64, cpr,         \
-      static_cast<TO *>(out), out_lse)
+  do {                                                                       \
+    if (S <= 4)                                                              \
+      merge_chunks_kernel<TI, TO, 4><<<cgrid, kChunkThreads, 0, stream>>>(   \
+          static_cast<const TI *>(parts_out), parts_lse, S, rows64, cpr,     \
+          static_cast<TO *>(out), out_lse);                                  \
+    else                                                                     \
+      merge_chunks_kernel<TI, TO, 8><<<cgrid, kChunkThreads, 0, stream>>>(   \
+          static_cast<const TI *>(parts_out), parts_lse, S, rows64, cpr,     \
+          static_cast<TO *>(out), out_lse);                                  \
+  } while (0)
     if (parts_dtype == MLA_BF16 && out_dtype == MLA_BF16) MLA_MERGE_C(__nv_bfloat16, __nv_bfloat16);
     else if (parts_dtype == MLA_BF16) MLA_MERGE_C(__nv_bfloat16, float);
     else if (out_dtype == MLA_BF16) MLA_MERGE_C(float, __nv_bfloat16);
