@@ -7,17 +7,21 @@
 // merged by LSE) and §MLA Prefill vs Decode (prefill uses expanded heads:
 // QK width 128 + 64 = 192, V width 128).
 //
-// One CTA per (128 query rows, head, request).  Per 128-key tile:
-//   S = Q K^T   tcgen05 M=128 N=128 K=192 (12 MMAs) into a TMEM buffer,
-//   P = exp2(S*scale*log2e - m) as bf16 written back over S in TMEM,
-//   O += P V    tcgen05 with A = P from TMEM, B = V (MN-major) from smem.
-// TMEM: S/P double buffer [0,256), O [256,384).  K (48 KB) and V (32 KB)
-// tiles have rings of their own, two stages each: a K stage is refilled as
-// soon as the QK that read it is done, a tile and a half before P.V frees
-// the V stage of the same tile, so the next K tiles are in flight while the
-// softmax runs; the tiles a few steps further ahead are pulled into L2 by
-// tensor prefetches.  Warp 0 = TMA, warp 1 = MMA, warps 2..5 = softmax +
-// epilogue (one query row per thread); lazy O rescaling.
+// One CTA per (256 query rows, head, request): two query tiles A and B of
+// 128 rows share every K / V tile.  Per 128-key tile and query tile g:
+//   S_g = Q_g K^T   tcgen05 M=128 N=128 K=192 (12 MMAs) into TMEM,
+//   P_g = exp2(S_g*scale*log2e - m) as bf16 written back over S_g in TMEM,
+//   O_g += P_g V    tcgen05 with A = P_g from TMEM, B = V (MN-major).
+// The two tiles ping-pong on the tensor core: while one softmax warpgroup
+// turns S_A into P_A, the tensor core runs P.V and the next QK of tile B,
+// and the other way round, so neither the softmax nor the tensor core waits
+// for the other in steady state; each K / V tile is read into the SM once
+// for 256 queries.  TMEM: [S_A | O_A | S_B | O_B], 128 columns each.  A
+// 2-stage K ring (48 KB tiles: a stage refills once both QKs of its tile
+// are done) and one V stage (32 KB, refilled once both P.Vs are done); the
+// tiles four ahead are pulled into L2 by tensor prefetches.  Warp 0 = TMA,
+// warp 1 = MMA, warps 2..5 = softmax + epilogue of tile A, warps 6..9 of
+// tile B (one query row per thread); lazy O rescaling.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -36,18 +40,22 @@ __device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap *map, int x, i
                : "memory");
 }
 
-constexpr int kBM = 128, kBN = 128;
+constexpr int kBM = 128, kBN = 128;              // query rows per tile, keys per tile
+constexpr int kQT = 2;                           // query tiles per CTA
 constexpr int kDq = 192, kDv = 128;
 constexpr int kBox = 128 * 128;                  // 128 rows x 64 bf16
 constexpr int kQBytes = 3 * kBox;                // 48 KB
 constexpr int kKBytes = 3 * kBox;                // 48 KB
 constexpr int kVBytes = 2 * kBox;                // 32 KB
-constexpr int kStages = 2;                       // per ring (K and V)
+constexpr int kKStages = 2;
 constexpr int kPrefetchAhead = 4;                // tiles pulled into L2 ahead
-constexpr int kSmemBytes = kQBytes + kStages * (kKBytes + kVBytes) + 256 + 1024;
-constexpr int kThreads = 192;
-constexpr uint32_t kColS = 0, kColO = 256;
+constexpr int kOffK = kQT * kQBytes;
+constexpr int kOffV = kOffK + kKStages * kKBytes;
+constexpr int kOffBars = kOffV + kVBytes;
+constexpr int kSmemBytes = kOffBars + 256 + 1024;
+constexpr int kThreads = 320;
 constexpr float kRescaleLog2 = 8.f;
+static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 
 struct PrefillArgs {
   const int32_t *cu_q, *cu_k;
@@ -61,51 +69,65 @@ __device__ __forceinline__ uint32_t pack2(float a, float b) {
   return bf16x2_rn(a, b);
 }
 
+// Key tiles visible to query tile [row0, row0 + rows) of a request with nq
+// queries and nk keys (the causal mask aligns the last query with the last key).
+__device__ __forceinline__ int tiles_for(int row0, int rows, int nq, int nk, int causal) {
+  if (rows <= 0) return 0;
+  int key_end = nk;
+  if (causal) key_end = min(nk, row0 + rows - 1 + nk - nq + 1);
+  key_end = max(key_end, 0);
+  return (key_end + kBN - 1) / kBN;
+}
+
+// 10 warps: blocks are given registers in units of four warps, so 12 warps'
+// worth (at most 168 registers a thread)
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
                const __grid_constant__ CUtensorMap tm_k,
                const __grid_constant__ CUtensorMap tm_v, PrefillArgs args,
                int *err) {
-  const int qt = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int qp = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int q0 = __ldg(args.cu_q + b), nq = __ldg(args.cu_q + b + 1) - q0;
   const int k0 = __ldg(args.cu_k + b), nk = __ldg(args.cu_k + b + 1) - k0;
-  if (qt * kBM >= nq) return;  // uniform across the CTA: nothing allocated yet
-  const int rows = min(kBM, nq - qt * kBM);
-  // keys visible to the last row of this tile
-  int key_end = nk;
-  if (args.causal) key_end = min(nk, qt * kBM + rows - 1 + nk - nq + 1);
-  key_end = max(key_end, 0);
-  const int ntiles = (key_end + kBN - 1) / kBN;
+  if (qp * kQT * kBM >= nq) return;  // uniform across the CTA: nothing allocated yet
+  int rows_g[kQT], nt_g[kQT];
+#pragma unroll
+  for (int g = 0; g < kQT; ++g) {
+    const int row0 = (qp * kQT + g) * kBM;
+    rows_g[g] = max(0, min(kBM, nq - row0));
+    nt_g[g] = tiles_for(row0, rows_g[g], nq, nk, args.causal);
+  }
+  const int ntiles = max(nt_g[0], nt_g[1]);
 
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t *sm_q = smem;
-  uint8_t *sm_k = smem + kQBytes;                      // [kStages] K tiles
-  uint8_t *sm_v = sm_k + kStages * kKBytes;            // [kStages] V tiles
-  uint64_t *bars = reinterpret_cast<uint64_t *>(sm_v + kStages * kVBytes);
-  uint64_t *k_full = bars, *k_empty = bars + kStages;
-  uint64_t *v_full = bars + 2 * kStages, *v_empty = bars + 3 * kStages;
-  uint64_t *s_full = bars + 4 * kStages, *p_full = s_full + 2;
-  uint64_t *pv_done = p_full + 2;             // [2], one per S/P buffer
-  uint64_t *q_full = pv_done + 2, *drain = q_full + 1;
+  uint8_t *sm_q = smem;                        // [kQT] query tiles
+  uint8_t *sm_k = smem + kOffK;                // [kKStages] K tiles
+  uint8_t *sm_v = smem + kOffV;                // the V tile
+  uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBars);
+  uint64_t *k_full = bars, *k_empty = bars + kKStages;
+  uint64_t *v_full = bars + 2 * kKStages, *v_empty = v_full + 1;
+  uint64_t *s_full = v_empty + 1;              // [kQT]
+  uint64_t *p_full = s_full + kQT;             // [kQT]
+  uint64_t *pv_done = p_full + kQT;            // [kQT]
+  uint64_t *q_full = pv_done + kQT, *drain = q_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(drain + 1);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   const int warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kStages; ++s) {
+    for (int s = 0; s < kKStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&k_empty[s], 1);
-      mbar_init(&v_full[s], 1);
-      mbar_init(&v_empty[s], 1);
     }
-    for (int s = 0; s < 2; ++s) {
-      mbar_init(&s_full[s], 1);
-      mbar_init(&p_full[s], 128);
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
+    for (int g = 0; g < kQT; ++g) {
+      mbar_init(&s_full[g], 1);
+      mbar_init(&p_full[g], 128);
+      mbar_init(&pv_done[g], 1);
     }
-    mbar_init(&pv_done[0], 1);
-    mbar_init(&pv_done[1], 1);
     mbar_init(q_full, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -121,28 +143,31 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------ TMA producer
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_k);
     prefetch_tmap(&tm_v);
     bool ok = true;
-    int t = 0;
+    int kt = 0, vt = 0;
     if (ntiles > 0) {
-      mbar_arrive_expect_tx(q_full, kQBytes);
-      for (int d = 0; d < 3; ++d)
-        tma_load_3d(sm_q + d * kBox, &tm_q, q_full, 64 * d, h, q0 + qt * kBM);
+      mbar_arrive_expect_tx(q_full, (rows_g[1] > 0 ? 2 : 1) * kQBytes);
+      for (int g = 0; g < kQT; ++g) {
+        if (rows_g[g] == 0) continue;
+        for (int d = 0; d < 3; ++d)
+          tma_load_3d(sm_q + g * kQBytes + d * kBox, &tm_q, q_full, 64 * d, h,
+                      q0 + (qp * kQT + g) * kBM);
+      }
     }
-    // K of tile t, then V of tile t - 1: K stages free up a tile and a
-    // half before the V stages of the same tiles
     auto load_k = [&](int u) -> bool {
-      const int s = u % kStages;
-      if (u >= kStages && !mbar_wait(&k_empty[s], ((u / kStages) - 1) & 1, abort_flag))
+      const int s = u % kKStages;
+      if (u >= kKStages && !mbar_wait(&k_empty[s], ((u / kKStages) - 1) & 1, abort_flag))
         return false;
       mbar_arrive_expect_tx(&k_full[s], kKBytes);
       const int row = k0 + u * kBN;
       for (int d = 0; d < 3; ++d)
         tma_load_3d(sm_k + s * kKBytes + d * kBox, &tm_k, &k_full[s], 64 * d, h, row);
-      // the tiles further ahead go to L2 now (the rings hold only two)
-      for (int a = (u == 0 ? kStages : kPrefetchAhead); a <= kPrefetchAhead; ++a) {
+      // the tiles further ahead go to L2 now (the rings hold one or two)
+      for (int a = (u == 0 ? 1 : kPrefetchAhead); a <= kPrefetchAhead; ++a) {
         if (u + a < ntiles) {
           const int prow = k0 + (u + a) * kBN;
           for (int d = 0; d < 3; ++d) tma_prefetch_3d(&tm_k, 64 * d, h, prow);
@@ -152,71 +177,86 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       return true;
     };
     auto load_v = [&](int u) -> bool {
-      const int s = u % kStages;
-      if (u >= kStages && !mbar_wait(&v_empty[s], ((u / kStages) - 1) & 1, abort_flag))
-        return false;
-      mbar_arrive_expect_tx(&v_full[s], kVBytes);
+      if (u >= 1 && !mbar_wait(v_empty, (u - 1) & 1, abort_flag)) return false;
+      mbar_arrive_expect_tx(v_full, kVBytes);
       const int row = k0 + u * kBN;
-      for (int d = 0; d < 2; ++d)
-        tma_load_3d(sm_v + s * kVBytes + d * kBox, &tm_v, &v_full[s], 64 * d, h, row);
+      for (int d = 0; d < 2; ++d) tma_load_3d(sm_v + d * kBox, &tm_v, v_full, 64 * d, h, row);
       return true;
     };
-    int tv = 0;
-    for (; ok && t < ntiles; ++t) {
-      if (!(ok = load_k(t))) break;
-      if (t >= 1 && !(ok = load_v(tv++))) break;
+    // K(0), K(1), V(0), then per tile t: K(t+1) (its stage frees when both
+    // QKs of tile t-1 are done) before V(t) (free when both P.Vs of t-1 are)
+    for (; ok && kt < min(ntiles, kKStages); ++kt) ok = load_k(kt);
+    for (; ok && vt < ntiles; ++vt) {
+      if (vt >= 1 && kt < ntiles && kt == vt + 1) {
+        if (!(ok = load_k(kt))) break;
+        ++kt;
+      }
+      if (!(ok = load_v(vt))) break;
     }
-    for (; ok && tv < ntiles; ++tv) ok = load_v(tv);
     if (*abort_flag) {
       volatile int no_abort = 0;
-      for (int k = max(0, t - kStages); k < t; ++k)
-        mbar_wait(&k_full[k % kStages], (k / kStages) & 1, &no_abort);
-      for (int k = max(0, tv - kStages); k < tv; ++k)
-        mbar_wait(&v_full[k % kStages], (k / kStages) & 1, &no_abort);
+      for (int k = max(0, kt - kKStages); k < kt; ++k)
+        mbar_wait(&k_full[k % kKStages], (k / kKStages) & 1, &no_abort);
+      if (vt > 0) mbar_wait(v_full, (vt - 1) & 1, &no_abort);
       if (ntiles > 0) mbar_wait(q_full, 0, &no_abort);
     }
   } else if (warp == 1 && lane == 0) {
+    // ----------------------------------------------------------- MMA
     const uint32_t idesc_qk = idesc_bf16(128, kBN, false, false);
     const uint32_t idesc_pv = idesc_bf16(128, kDv, false, true);
-    const uint32_t qa = smem_u32(sm_q);
     bool ok = ntiles == 0 || mbar_wait(q_full, 0, abort_flag);
-    auto issue_qk = [&](int t) {
-      const uint32_t kb = smem_u32(sm_k + (t % kStages) * kKBytes);
-      const uint32_t d = tmem + kColS + 128 * (t & 1);
+    auto issue_qk = [&](int g, int t) {
+      const uint32_t qa = smem_u32(sm_q + g * kQBytes);
+      const uint32_t kb = smem_u32(sm_k + (t % kKStages) * kKBytes);
+      const uint32_t d = tmem + 256 * g;
 #pragma unroll
       for (int k = 0; k < kDq / 16; ++k)
         mma_f16_ss(d, sdesc(qa + (k >> 2) * kBox + (k & 3) * 32, 16, 1024, kSwizzle128B),
                    sdesc(kb + (k >> 2) * kBox + (k & 3) * 32, 16, 1024, kSwizzle128B),
                    idesc_qk, k > 0);
-      mma_commit(&s_full[t & 1]);
-      mma_commit(&k_empty[t % kStages]);   // the K stage is read
+      mma_commit(&s_full[g]);
     };
-    if (ok && ntiles > 0) {
-      ok = mbar_wait(&k_full[0], 0, abort_flag);
-      if (ok) {
-        tc_fence_after();
-        issue_qk(0);
-      }
-    }
-    for (int t = 0; ok && t < ntiles; ++t) {
-      if (t + 1 < ntiles) {
-        if (!(ok = mbar_wait(&k_full[(t + 1) % kStages], ((t + 1) / kStages) & 1, abort_flag)))
-          break;
-        tc_fence_after();
-        issue_qk(t + 1);
-      }
-      if (!(ok = mbar_wait(&p_full[t & 1], (t >> 1) & 1, abort_flag) &&
-                 mbar_wait(&v_full[t % kStages], (t / kStages) & 1, abort_flag)))
-        break;
-      tc_fence_after();
-      const uint32_t vb = smem_u32(sm_v + (t % kStages) * kVBytes);
+    auto issue_pv = [&](int g, int t) {
+      const uint32_t vb = smem_u32(sm_v);
 #pragma unroll
       for (int kk = 0; kk < kBN / 16; ++kk)
-        mma_f16_ts(tmem + kColO, tmem + kColS + 128 * (t & 1) + 8 * kk,
+        mma_f16_ts(tmem + 256 * g + 128, tmem + 256 * g + 8 * kk,
                    sdesc(vb + kk * 2048, kBox, 1024, kSwizzle128B), idesc_pv,
                    (t > 0 || kk > 0) ? 1u : 0u);
-      mma_commit(&v_empty[t % kStages]);
-      mma_commit(&pv_done[t & 1]);
+      mma_commit(&pv_done[g]);
+    };
+    // Tile 0's QKs; then per tile t: P.V_A(t), QK_A(t+1), P.V_B(t),
+    // QK_B(t+1).  QK_g(t+1) overwrites S_g after P.V_g(t) has read P_g from
+    // the same columns (the tensor core runs one thread's MMAs in order).
+    if (ok && ntiles > 0 && (ok = mbar_wait(&k_full[0], 0, abort_flag))) {
+      tc_fence_after();
+      for (int g = 0; g < kQT; ++g)
+        if (nt_g[g] > 0) issue_qk(g, 0);
+      mma_commit(&k_empty[0]);
+    }
+    for (int t = 0; ok && t < ntiles; ++t) {
+      if (!(ok = mbar_wait(v_full, t & 1, abort_flag))) break;
+      bool k_next = false;   // K(t+1) has landed
+      for (int g = 0; g < kQT; ++g) {
+        if (t < nt_g[g]) {
+          if (!(ok = mbar_wait(&p_full[g], t & 1, abort_flag))) break;
+          tc_fence_after();
+          issue_pv(g, t);
+        }
+        if (g == kQT - 1) mma_commit(v_empty);   // both P.Vs of tile t issued
+        if (t + 1 < nt_g[g]) {
+          if (!k_next) {
+            if (!(ok = mbar_wait(&k_full[(t + 1) % kKStages], ((t + 1) / kKStages) & 1,
+                                 abort_flag)))
+              break;
+            tc_fence_after();
+            k_next = true;
+          }
+          issue_qk(g, t + 1);
+        }
+      }
+      if (!ok) break;
+      if (k_next) mma_commit(&k_empty[(t + 1) % kKStages]);   // both QKs of tile t+1 issued
     }
     if (!ok) {
       mma_commit(drain);
@@ -224,23 +264,26 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
       mbar_wait(drain, 0, &no_abort);
     }
   } else if (warp >= 2) {
+    // ------------------------------------------- softmax + epilogue of tile g
+    const int g = (warp - 2) >> 2;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
-    const int i = qt * kBM + r;                      // query index in request
+    const uint32_t col_s = 256 * g, col_o = 256 * g + 128;
+    const int i = (qp * kQT + g) * kBM + r;         // query index in request
     const int lim = args.causal ? min(nk, i + nk - nq + 1) : nk;
+    const int n = nt_g[g];
     float m = -INFINITY, l = 0.f;
     bool ok = true;
-    for (int t = 0; t < ntiles; ++t) {
-      const int sb = t & 1;
-      if (!(ok = mbar_wait(&s_full[sb], (t >> 1) & 1, abort_flag))) break;
+    for (int t = 0; t < n; ++t) {
+      if (!(ok = mbar_wait(&s_full[g], t & 1, abort_flag))) break;
       tc_fence_after();
       // raw scores; only a tile that crosses this row's limit is masked
       float x[kBN];
 #pragma unroll
       for (int c = 0; c < kBN; c += 32) {
         uint32_t v[32];
-        tmem_ld_x32(lane_base + kColS + 128 * sb + c, v);
+        tmem_ld_x32(lane_base + col_s + c, v);
 #pragma unroll
         for (int k = 0; k < 32; ++k) x[c + k] = __uint_as_float(v[k]);
       }
@@ -258,19 +301,19 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         const float m_new = fmaxf(m, tmax);
         const bool need = m_new > m + kRescaleLog2 || (m == -INFINITY && m_new > -INFINITY);
         if (__any_sync(0xffffffffu, need)) {
-          // rescale only after PV(t-1) landed; per-buffer barriers are never
-          // more than one phase ahead of this wait (see the decode kernel)
-          if (!(ok = mbar_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, abort_flag))) break;
+          // rescale only after P.V(t-1) landed; the barrier is never more
+          // than one phase ahead of this wait (P.V(t) needs this tile's P)
+          if (!(ok = mbar_wait(&pv_done[g], (t - 1) & 1, abort_flag))) break;
           tc_fence_after();
           const float alpha = need ? (m == -INFINITY ? 0.f : ex2(m - m_new)) : 1.f;
 #pragma unroll 1
           for (int c = 0; c < kDv; c += 32) {
             uint32_t o[32];
-            tmem_ld_x32(lane_base + kColO + c, o);
+            tmem_ld_x32(lane_base + col_o + c, o);
 #pragma unroll
             for (int k = 0; k < 32; ++k)
               o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-            tmem_st_x32(lane_base + kColO + c, o);
+            tmem_st_x32(lane_base + col_o + c, o);
           }
           l *= alpha;
           if (need) m = m_new;
@@ -299,24 +342,23 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
         uint32_t pk[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) pk[k] = pack2(x[c + 2 * k], x[c + 2 * k + 1]);
-        tmem_st_x32(lane_base + kColS + 128 * sb + c / 2, pk);
+        tmem_st_x32(lane_base + col_s + c / 2, pk);
       }
       l += psum;
       tc_fence_before();
-      mbar_arrive(&p_full[sb]);
+      mbar_arrive(&p_full[g]);
     }
-    if (ok && ntiles > 0)
-      ok = mbar_wait(&pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, abort_flag);
+    if (ok && n > 0) ok = mbar_wait(&pv_done[g], (n - 1) & 1, abort_flag);
     tc_fence_after();
-    if (ok) {
-      const bool row_ok = r < rows;
+    if (ok && rows_g[g] > 0) {
+      const bool row_ok = r < rows_g[g];
       const int64_t orow = static_cast<int64_t>(q0 + i) * args.H + h;
       const bool empty = !(l > 0.f);
       const float inv = empty ? 0.f : 1.f / l;
 #pragma unroll 1
       for (int c = 0; c < kDv; c += 32) {
         uint32_t o[32];
-        if (ntiles > 0) tmem_ld_x32(lane_base + kColO + c, o);
+        if (n > 0) tmem_ld_x32(lane_base + col_o + c, o);
         if (!row_ok) continue;
         uint4 *dst = reinterpret_cast<uint4 *>(args.out + orow * kDv + c);
 #pragma unroll
@@ -324,7 +366,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tm_q,
           float v[8];
 #pragma unroll
           for (int e = 0; e < 8; ++e)
-            v[e] = (ntiles > 0 && !empty) ? __uint_as_float(o[8 * k + e]) * inv : 0.f;
+            v[e] = (n > 0 && !empty) ? __uint_as_float(o[8 * k + e]) * inv : 0.f;
           dst[k] = make_uint4(pack2(v[0], v[1]), pack2(v[2], v[3]), pack2(v[4], v[5]),
                               pack2(v[6], v[7]));
         }
@@ -390,7 +432,7 @@ extern "C" int mla_prefill_attn(const void *q, const void *k, const void *v,
   if (cudaFuncSetAttribute(prefill_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            kSmemBytes) != cudaSuccess)
     return MLA_ERR_CUDA;
-  dim3 grid((max_q_len + kBM - 1) / kBM, H, B);
+  dim3 grid((max_q_len + kQT * kBM - 1) / (kQT * kBM), H, B);
   prefill_kernel<<<grid, kThreads, kSmemBytes, stream>>>(tq, tk, tv, a, err);
   return launch_status();
 }
