@@ -130,7 +130,7 @@ def whole_job_rate(units_per_rank, world, ms_max):
 
 def make_inputs(device):
     import synth
-    case = synth.config2(B=B, ctx=CTX)
+    case = synth.dsv3_decode(B=B, ctx=CTX)
     d = dict(
         q_nope=case.q_nope.to(device), q_pe=case.q_pe.to(device),
         w_uk_t=case.w_uk_t.to(device), w_uv=case.w_uv.to(device),
@@ -388,7 +388,7 @@ def run_extras(device, flush, reps=10, only=None):
 
     # long single request: 131072 tokens as 8 explicit shards, merged
     if want("long"):
-        c3 = synth.config3()
+        c3 = synth.long_request()
         S = 8
         q3 = c3.q.to(device).expand(S, 1, 128, 576).contiguous()
         bt3, sl3 = i32(np.repeat(c3.block_table, S, axis=0)), i32(np.repeat(c3.seq_lens, S))
@@ -413,7 +413,7 @@ def run_extras(device, flush, reps=10, only=None):
 
     # fp8 KV cache: B = 64, ctx U[1024, 16384], e4m3 cache and query
     if want("fp8"):
-        c4 = synth.config4()
+        c4 = synth.fp8_decode()
         q4, cache4 = c4.q.to(device), c4.cache.to(device)
         bt4, sl4 = i32(c4.block_table), i32(c4.seq_lens)
         ws4 = torch.empty(m.mla_decode_workspace_size(c4.B, 1, 128, bt4.shape[1] * 64),
@@ -432,7 +432,7 @@ def run_extras(device, flush, reps=10, only=None):
 
     # speculative decode: B = 128, q_len 2 (causal pair), lognormal contexts
     if want("spec"):
-        c5 = synth.config5_decode()
+        c5 = synth.spec_decode()
         q5, cache5 = c5.q.to(device), c5.cache.to(device)
         bt5, sl5 = i32(c5.block_table), i32(c5.seq_lens)
         ws5 = torch.empty(m.mla_decode_workspace_size(c5.B, 2, 128, bt5.shape[1] * 64),
@@ -456,7 +456,7 @@ def run_extras(device, flush, reps=10, only=None):
     # chunked-prefill context step: 4 x 8192 context rows on 4 interleaved
     # shards, 512 new tokens each, H = 128
     if want("prefill"):
-        cp = synth.config5_prefill()
+        cp = synth.context_prefill()
         smb = max(s_[1].shape[1] for s_ in cp.shards)
         tables = []
         for _, sbt, _ in cp.shards:
@@ -537,7 +537,7 @@ def oracle_sample(n_req):
     """fp64 oracle on n_req requests of the workload; returns (seconds, tokens)."""
     import synth
     from oracle import codecs, mla as O
-    case = synth.config2(B=B, ctx=CTX)
+    case = synth.dsv3_decode(B=B, ctx=CTX)
     f = lambda t: codecs.bf16_to_f64(t.view(torch.int16).numpy())
     qn, qp = f(case.q_nope)[:n_req], f(case.q_pe)[:n_req]
     wk, wv = f(case.w_uk_t), f(case.w_uv)

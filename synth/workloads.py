@@ -38,8 +38,8 @@ __all__ = [
     "BLOCK", "KV_LORA", "ROPE", "QK_NOPE", "V_HEAD", "D_QK",
     "generator", "as_bf16", "as_e4m3", "paged_layout", "fill_cache",
     "DecodeCase", "PrefillCase", "decode_case", "prefill_case",
-    "config1", "config2", "config3", "config4", "config5_decode",
-    "config5_prefill", "even_shards", "shard_cache_interleaved",
+    "tiny_decode", "dsv3_decode", "long_request", "fp8_decode", "spec_decode",
+    "context_prefill", "even_shards", "shard_cache_interleaved",
     "BF16_NAN_BITS", "E4M3_NAN_BITS",
 ]
 
@@ -194,7 +194,7 @@ def decode_case(name, seed, *, B, H, seq_lens, q_len=1, kv_dtype="bf16",
                       w_uk_t, w_uv, shards)
 
 
-def config1(poison=True):
+def tiny_decode(poison=True):
     """Tiny: B=2, H=16, ctx 37 and 130, 2 shards, N(0,1)/sqrt(dim) values."""
     return decode_case(
         "tiny_b2_h16_ctx37_130", 1001, B=2, H=16, seq_lens=[37, 130],
@@ -204,19 +204,19 @@ def config1(poison=True):
         w_uv_std=1.0 / math.sqrt(512), n_shards=2, poison=poison)
 
 
-def config2(poison=False, B=32, ctx=4096):
+def dsv3_decode(poison=False, B=32, ctx=4096):
     """DeepSeek-V3 decode shape: B=32, H=128, ctx 4096, cache N(0,1)."""
     return decode_case("dsv3_b32_h128_ctx4096", 1002, B=B, H=128,
                        seq_lens=[ctx] * B, poison=poison)
 
 
-def config3(poison=False, ctx=131072):
+def long_request(poison=False, ctx=131072):
     """Long single request: ctx 131072, 8 equal shards then a merge."""
     return decode_case("long_b1_h128_ctx131072", 1003, B=1, H=128,
                        seq_lens=[ctx], n_shards=8, poison=poison)
 
 
-def config4(poison=False, B=64, lo=1024, hi=16384):
+def fp8_decode(poison=False, B=64, lo=1024, hi=16384):
     """FP8 KV: B=64, ctx ~ U[1024,16384], e4m3 cache and query."""
     g = generator(2004)
     lens = g.integers(lo, hi, size=B, endpoint=True)
@@ -230,7 +230,7 @@ def lognormal_lengths(g, n, median=2048.0, sigma=1.0, lo=2, hi=32768):
     return np.clip(x, lo, hi).astype(np.int32)
 
 
-def config5_decode(poison=False, B=128):
+def spec_decode(poison=False, B=128):
     """Speculative decode: B=128, q_len=2 causal, ctx lognormal(ln 2048, 1)."""
     lens = lognormal_lengths(generator(2005), B)
     return decode_case("spec_b128_q2_h128_lognormal", 1005, B=B, H=128,
@@ -312,7 +312,7 @@ def prefill_case(name, seed, *, ctx_lens, new_lens, H=128, W=4, interleave=1,
                        1.0 / math.sqrt(QK_NOPE + ROPE))
 
 
-def config5_prefill(poison=False, ctx=8192, n_req=4, sq=512, H=128):
+def context_prefill(poison=False, ctx=8192, n_req=4, sq=512, H=128):
     """Chunked-prefill context step: 4 x 8192 context rows on 4 interleaved
     shards, 512 new tokens per request, W_kvb ~ N(0, 0.02)."""
     return prefill_case("prefill_4x8192_w4_sq512", 1055, ctx_lens=[ctx] * n_req,

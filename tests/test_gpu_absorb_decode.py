@@ -109,7 +109,7 @@ def test_plan_is_valid(m, split_tiles, n_groups, fp8):
                                               (128, 2, 76)])
 def test_plan_is_valid_many_jobs(m, B, q_len, n_groups):
     """Up to J = 400 jobs: the one-warp plan kernel (J <= 256) and the
-    block-scan plan kernel beyond it; the config-2 and config-5 shapes."""
+    block-scan plan kernel beyond it; the DeepSeek-V3 decode and speculative decode shapes."""
     g = synth.generator(431 + B)
     H = 128
     seq = g.integers(0, 5000, B).astype(np.int32)
@@ -161,10 +161,10 @@ def _check(out, lse, ro, rl, t, out_tol=OUT_TOL, lse_tol=LSE_TOL, label="decode"
                     label=label)
 
 
-def test_decode_config1_tiny(m):
-    case = synth.config1(poison=True)
+def test_decode_tiny(m):
+    case = synth.tiny_decode(poison=True)
     out, lse = _run_decode(m, case)
-    _check(out, lse, *_oracle_decode(case), label="config 1")
+    _check(out, lse, *_oracle_decode(case), label="tiny decode")
     assert m.mla_get_device_error() == 0
 
 
@@ -191,9 +191,9 @@ def test_decode_causal_pair(m):
 
 
 def test_decode_explicit_shards_then_merge(m):
-    """Config-1 shape: 2 shards per request via kv_starts/kv_ends, merged by
+    """Tiny decode shape: 2 shards per request via kv_starts/kv_ends, merged by
     mla_merge_states, equals the unsplit decode."""
-    case = synth.config1(poison=True)
+    case = synth.tiny_decode(poison=True)
     B = case.B
     parts_o, parts_l = [], []
     for s in range(2):
@@ -241,10 +241,10 @@ def test_decode_peaked_scores(m):
     _check(out, lse, ro, rl, t, out_tol=OUT_TOL + 2.0 ** -8 * float(np.abs(ro).max()))
 
 
-def test_chain_absorb_decode_vup_config2_sampled(m):
+def test_chain_absorb_decode_vup_dsv3_sampled(m):
     """DeepSeek-V3 decode shape (B=32, H=128, ctx 4096) end to end; the
     oracle checks 4 requests in full (the GPU runs all 32)."""
-    case = synth.config2()
+    case = synth.dsv3_decode()
     q = m.mla_absorb_q(case.q_nope.cuda(), case.q_pe.cuda(), case.w_uk_t.cuda())
     q = q.view(case.B, 1, case.H, 576)
     out, lse = m.mla_decode_paged(q, case.cache.cuda(), _i32(case.block_table),
@@ -257,7 +257,7 @@ def test_chain_absorb_decode_vup_config2_sampled(m):
     # stage by stage: the decode against the oracle fed the GPU's own query
     ro, rl = O.paged_decode(qo, cache, bt, sl, case.sm_scale)
     t = decode_terms(qo, cache, bt, sl, case.sm_scale)
-    _check(out[pick], lse[pick], ro, rl, t, label="config 2 decode")
+    _check(out[pick], lse[pick], ro, rl, t, label="DeepSeek-V3 decode")
     ref_y = O.v_up(f64(out)[pick][:, 0], f64(case.w_uv))
     abs_sum = np.einsum("thl,hvl->thv", np.abs(f64(out)[pick][:, 0]), np.abs(f64(case.w_uv)))
     assert np.all(np.abs(f64(y)[pick] - ref_y) <= gemm_tolerance(ref_y, abs_sum))
@@ -270,10 +270,10 @@ def test_chain_absorb_decode_vup_config2_sampled(m):
     assert np.all(np.abs(lse.cpu().numpy()[pick] - el) <= LSE_TOL + np.abs(rl - el))
 
 
-def test_decode_config3_long_shards(m):
+def test_decode_long_request_shards(m):
     """ctx 131072 as 8 explicit shards (one launch, B'=8 shard rows) merged
     on the GPU, against the unsplit oracle."""
-    case = synth.config3()
+    case = synth.long_request()
     S = 8
     q = case.q.cuda().expand(S, 1, case.H, 576).contiguous()
     bt = np.repeat(case.block_table, S, axis=0)
@@ -287,16 +287,16 @@ def test_decode_config3_long_shards(m):
                                 out_dtype=torch.bfloat16)
     ro, rl, t = _oracle_decode(case)
     _check(mo, ml, ro.reshape(1, case.H, 512), rl.reshape(1, case.H),
-           t.take((slice(None), 0)), label="config 3")
+           t.take((slice(None), 0)), label="long request")
 
 
-def test_decode_config5_sampled(m):
+def test_decode_spec_sampled(m):
     """Spec decode shape (B=128, q_len 2, lognormal ctx): all requests run,
     12 are checked in full by the oracle."""
-    case = synth.config5_decode()
+    case = synth.spec_decode()
     out, lse = _run_decode(m, case)
     pick = [0, 1, 5, 17, 33, 50, 64, 77, 90, 101, 120, 127]
-    _check(out[pick], lse[pick], *_oracle_decode(case, pick=pick), label="config 5 decode")
+    _check(out[pick], lse[pick], *_oracle_decode(case, pick=pick), label="speculative decode")
 
 
 def test_decode_reruns_bit_identical(m):
@@ -305,7 +305,7 @@ def test_decode_reruns_bit_identical(m):
     cross job boundaries, partial merges) exercises every hand-off of the
     paired-CTA kernel; a hand-off that is not ordered shows up as a rerun
     that differs (this is how a staging-buffer race was caught)."""
-    case = synth.config5_decode()
+    case = synth.spec_decode()
     out0, lse0 = _run_decode(m, case)
     ob0, lb0 = bits(out0), bits(lse0)
     for _ in range(40):
@@ -352,11 +352,11 @@ def test_decode_fp8_causal_pair_head_groups(m):
            label="fp8 pair")
 
 
-def test_decode_config4_fp8_sampled(m):
+def test_decode_fp8_sampled(m):
     """FP8 KV shape (B=64, ctx U[1024,16384], e4m3 cache and query with
     per-tensor scales): all requests run, 6 are checked in full."""
-    case = synth.config4()
+    case = synth.fp8_decode()
     out, lse = _run_decode(m, case)
     pick = [0, 9, 21, 40, 52, 63]
     _check(out[pick], lse[pick], *_oracle_decode(case, pick=pick), out_tol=FP8_OUT_TOL,
-           lse_tol=FP8_LSE_TOL, label="config 4")
+           lse_tol=FP8_LSE_TOL, label="fp8 decode")

@@ -148,7 +148,7 @@ def test_bounded_wait_timeout_is_reported_and_context_survives(m):
     m.mla_get_device_error()                     # start from a clear word
     m.mla_selftest_wait_timeout(2_000_000)
     assert m.mla_get_device_error() & 8
-    case = synth.config1(poison=True)
+    case = synth.tiny_decode(poison=True)
     out, lse = m.mla_decode_paged(
         case.q.cuda(), case.cache.cuda(),
         torch.as_tensor(case.block_table, dtype=torch.int32).cuda(),

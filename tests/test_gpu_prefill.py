@@ -1,5 +1,5 @@
 """GPU parity of the chunked-prefill context step: kv_b_proj expansion,
-prefill attention (causal / non-causal, with LSE) and the full config-5
+prefill attention (causal / non-causal, with LSE) and the full DeepSeek-V3
 chain (sharded gather + reorg -> expand -> context attention, new-token
 causal attention -> merge) against the fp64 oracle."""
 
@@ -81,15 +81,15 @@ def test_prefill_no_visible_keys(m):
                     label="no visible keys")
 
 
-def test_chunked_prefill_config5_sampled(m):
-    """Config 5 context step at full size: 4 requests x 8192 context rows on
+def test_chunked_prefill_context_sampled(m):
+    """DeepSeek-V3 context step at full size: 4 requests x 8192 context rows on
     4 interleaved shards, 512 new tokens each, H = 128.  Stage by stage, each
     against the oracle fed the GPU's own inputs to that stage: gather+reorg
     (bit-exact), expand (GEMM bound), non-causal context attention and causal
     new-token attention (spec and scale-aware bounds), LSE merge; then
     end to end against the unrounded fp64 chain.  The oracle samples 2 heads
     x 16 query rows per request (it expands only those heads)."""
-    case = synth.config5_prefill()
+    case = synth.context_prefill()
     W, I, H = case.W, case.interleave, case.H
     ctx, new = case.ctx_lens, case.new_lens
     smb = max(s[1].shape[1] for s in case.shards)
@@ -138,14 +138,14 @@ def test_chunked_prefill_config5_sampled(m):
     tc = prefill_terms(qs, kc_s, vc_s, cu_q, cu_c, False, sc, q_rows)
     check_attention(f64(oc[:, heads])[q_rows], lc[:, heads].cpu().numpy()[q_rows], roc[q_rows],
                     rlc[q_rows], tc.take(q_rows), out_tol=OUT_TOL, lse_tol=LSE_TOL,
-                    label="config 5 context attention")
+                    label="context attention")
     # new-token causal attention on the GPU's own K/V
     kn_s, vn_s = f64(kn[:, heads]), f64(vn[:, heads])
     ron, rln = O.prefill_attention(qs, kn_s, vn_s, cu_q, cu_q, True, sc, q_rows)
     tn = prefill_terms(qs, kn_s, vn_s, cu_q, cu_q, True, sc, q_rows)
     check_attention(f64(on[:, heads])[q_rows], ln[:, heads].cpu().numpy()[q_rows], ron[q_rows],
                     rln[q_rows], tn.take(q_rows), out_tol=OUT_TOL, lse_tol=LSE_TOL,
-                    label="config 5 new-token attention")
+                    label="new-token attention")
     # the merge of the GPU's own two states
     po = np.stack([f64(oc[:, heads])[q_rows], f64(on[:, heads])[q_rows]])
     pl = np.stack([lc[:, heads].cpu().numpy()[q_rows], ln[:, heads].cpu().numpy()[q_rows]])

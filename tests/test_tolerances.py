@@ -98,7 +98,7 @@ def _emulate_split_decode(q, cache, block_table, seq_lens, sm_scale, seg=64):
 
 @pytest.fixture(scope="module")
 def tiny():
-    case = synth.config1(poison=False)
+    case = synth.tiny_decode(poison=False)
     q, cache = f64(case.q), f64(case.cache)
     ref_o, ref_l = O.paged_decode(q, cache, case.block_table, case.seq_lens, case.sm_scale)
     t = decode_terms(q, cache, case.block_table, case.seq_lens, case.sm_scale)
@@ -126,7 +126,7 @@ def test_bounds_admit_the_split_path_with_bf16_partials(tiny, seg):
 def test_bounds_reject_a_dropped_pv_tile(tiny):
     """Dropping the last 64-token tile's P.V step of the 130-token request
     (keeping the normaliser) stays far inside the 1e-2 max-abs tolerance at
-    config 1's magnitudes; the scale-aware bound catches it."""
+    the tiny decode's magnitudes; the scale-aware bound catches it."""
     case, q, cache, ref_o, ref_l, t = tiny
     o, l = _emulate_decode(q, cache, case.block_table, case.seq_lens, case.sm_scale,
                            drop_last_tile=True)
