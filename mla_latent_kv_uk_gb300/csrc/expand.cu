@@ -8,25 +8,17 @@
 //   [K_nope | V][n, h, 0:256] = kv[n, 0:512] . W_kvb[h*256 : h*256+256, :]^T
 //   K[n, h, 128:192]         = kv[n, 512:576]          (k_pe, broadcast)
 //
-// A dense GEMM (M = rows, N = H*256, K = 512) on tcgen05.  A persistent
-// grid of clusters of CL CTAs (CL = 4, 2 or 1, as many as the device keeps
-// resident) walks tiles of 128 rows x 256 columns (one head): the CTAs of a
-// cluster take consecutive 128-row blocks of the same head, so the head's
-// W_kvb chunk is fetched once per cluster — each CTA loads 1/CL of it and
-// TMA multicasts its piece to every CTA of the cluster — and the operand
-// reads from L2 drop from 384 KB per tile to 128 + 256/CL KB (each SM still
-// takes in the whole 384 KB).  64-wide K
-// chunks of both operands go through a 4-stage ring; a stage is refilled
-// only once the MMAs of every CTA of the cluster have read it (their
-// commits arrive on each CTA's empty barrier).  One thread issues M=128
-// N=256 K=16 MMAs into one of two TMEM accumulators, so the four epilogue
-// warps drain tile i while the tensor core computes tile i+1: 64-column
-// pieces go through two 128B-swizzled 16 KB staging buffers and leave as
-// tensor-map stores (whole 128-byte row pieces), and the k_pe columns are
-// copied row by row with coalesced 16-byte accesses.
+// A dense GEMM (M = rows, N = H*256, K = 512) on tcgen05: a persistent grid
+// of one CTA per SM walks tiles of 128 rows x 256 columns (one head),
+// consecutive CTAs on consecutive heads of the same rows, so the row blocks
+// and W_kvb (H*256 x 512) are read from L2.  64-wide K chunks of both
+// operands go through a 4-stage ring; one thread issues M=128 N=256 K=16
+// MMAs into one of two TMEM accumulators, so the four epilogue warps drain
+// tile i while the tensor core computes tile i+1: 64-column pieces go
+// through two 128B-swizzled 16 KB staging buffers and leave as tensor-map
+// stores (whole 128-byte row pieces), and the k_pe columns are copied row by
+// row with coalesced 16-byte accesses.
 #include <cuda_bf16.h>
-
-#include <mutex>
 
 #include "common.cuh"
 #include "sm100.cuh"
@@ -49,14 +41,13 @@ constexpr int kKChunks = 512 / 64;
 static_assert(kSmemBytes <= 232448, "shared memory of one CTA");
 
 struct ExpandArgs {
-  int N, H, m_tiles, tiles;   // tiles: cluster tiles (row-block groups x heads)
+  int N, H, m_tiles, tiles;   // tiles: row blocks x heads
   const __nv_bfloat16 *kv;    // [N, 576]
   __nv_bfloat16 *k_out;       // [N, H, 192]
 };
 
 __device__ __forceinline__ void epi_sync() { named_sync(1, 128); }
 
-template <int CL>
 __global__ void __launch_bounds__(kThreads, 1)
 expand_kernel(const __grid_constant__ CUtensorMap tm_a,
               const __grid_constant__ CUtensorMap tm_b,
@@ -74,15 +65,11 @@ expand_kernel(const __grid_constant__ CUtensorMap tm_a,
   volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_slot + 1);
   volatile int *go = abort_flag + 1;       // the epilogue warps' common decision
   const int warp = warp_id(), lane = lane_id();
-  const int rank = CL > 1 ? static_cast<int>(cluster_rank()) : 0;
-  const int cid = blockIdx.x / CL, ncl = gridDim.x / CL;
-  constexpr uint16_t kAll = static_cast<uint16_t>((1u << CL) - 1u);
-  constexpr int kPieceRows = 256 / CL;     // W_kvb rows this CTA fetches per chunk
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CL);   // the MMA commit of every CTA of the cluster
+      mbar_init(&empty[s], 1);
     }
     for (int s = 0; s < 2; ++s) {
       mbar_init(&acc_full[s], 1);
@@ -99,21 +86,16 @@ expand_kernel(const __grid_constant__ CUtensorMap tm_a,
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  // every CTA's barriers exist before any piece is multicast into it
-  if (CL > 1) cluster_sync();
   const uint32_t tmem = *tmem_slot;
 
-  // Cluster tile t: row-block group t / H (this CTA's block: group * CL +
-  // rank), head t % H.  Consecutive clusters take consecutive heads of the
-  // same rows, so the row blocks are read from L2 while W_kvb (H*256 x 512)
-  // stays L2-resident as well.
+  // tile t: row block t / H, head t % H (head-major inside a row block)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tm_a);
     prefetch_tmap(&tm_b);
     int kc = 0;
     bool ok = true;
-    for (int t = cid; ok && t < args.tiles; t += ncl) {
-      const int mt = (t / args.H) * CL + rank, h = t % args.H;
+    for (int t = blockIdx.x; ok && t < args.tiles; t += gridDim.x) {
+      const int mt = t / args.H, h = t % args.H;
       for (int c = 0; c < kKChunks; ++c, ++kc) {
         const int s = kc % kStages;
         if (kc >= kStages && !(ok = mbar_wait(&empty[s], ((kc / kStages) - 1) & 1, abort_flag)))
@@ -121,11 +103,7 @@ expand_kernel(const __grid_constant__ CUtensorMap tm_a,
         uint8_t *dst = smem + s * kStageBytes;
         mbar_arrive_expect_tx(&full[s], kStageBytes);
         tma_load_2d(dst, &tm_a, &full[s], c * 64, mt * 128);
-        if constexpr (CL > 1)
-          tma_load_2d_multicast(dst + kABytes + rank * kPieceRows * 128, &tm_b, &full[s], c * 64,
-                                h * 256 + rank * kPieceRows, kAll);
-        else
-          tma_load_2d(dst + kABytes, &tm_b, &full[s], c * 64, h * 256);
+        tma_load_2d(dst + kABytes, &tm_b, &full[s], c * 64, h * 256);
       }
     }
     if (*abort_flag) {
@@ -137,7 +115,7 @@ expand_kernel(const __grid_constant__ CUtensorMap tm_a,
     const uint32_t idesc = idesc_bf16(128, 256, false, false);
     int kc = 0, n = 0;
     bool ok = true;
-    for (int t = cid; ok && t < args.tiles; t += ncl, ++n) {
+    for (int t = blockIdx.x; ok && t < args.tiles; t += gridDim.x, ++n) {
       const int buf = n & 1;
       if (n >= 2 && !(ok = mbar_wait(&acc_empty[buf], ((n >> 1) - 1) & 1, abort_flag))) break;
       tc_fence_after();
@@ -153,9 +131,7 @@ expand_kernel(const __grid_constant__ CUtensorMap tm_a,
           mma_f16_ss(d, sdesc(a + kk * 32, 16, 1024, kSwizzle128B),
                      sdesc(b + kk * 32, 16, 1024, kSwizzle128B), idesc,
                      (c | kk) != 0);
-        // the stage is free for the cluster once every CTA's MMAs read it
-        if constexpr (CL > 1) mma_commit_multicast(&empty[s], kAll);
-        else mma_commit(&empty[s]);
+        mma_commit(&empty[s]);
       }
       if (ok) mma_commit(&acc_full[buf]);
     }
@@ -170,7 +146,7 @@ expand_kernel(const __grid_constant__ CUtensorMap tm_a,
     const int r = quarter * 32 + lane;         // accumulator row (TMEM lane)
     const uint32_t lane_base = tmem + ((quarter * 32u) << 16);
     int n = 0, box = 0;
-    for (int t = cid; t < args.tiles; t += ncl, ++n) {
+    for (int t = blockIdx.x; t < args.tiles; t += gridDim.x, ++n) {
       const int buf = n & 1;
       mbar_wait(&acc_full[buf], (n >> 1) & 1, abort_flag);
       // one decision for all four warps (a timed-out wait has set the flag
@@ -180,7 +156,7 @@ expand_kernel(const __grid_constant__ CUtensorMap tm_a,
       epi_sync();
       if (!*go) break;
       tc_fence_after();
-      const int mt = (t / args.H) * CL + rank, h = t % args.H;
+      const int mt = t / args.H, h = t % args.H;
       // four 64-column pieces: K nope [0,64) [64,128), V [0,64) [64,128)
 #pragma unroll 1
       for (int pc = 0; pc < 4; ++pc, ++box) {
@@ -205,9 +181,8 @@ expand_kernel(const __grid_constant__ CUtensorMap tm_a,
               bf16x2_rn(__uint_as_float(v[8 * c + 6]), __uint_as_float(v[8 * c + 7])));
         fence_proxy_async_smem();
         epi_sync();
-        // rows past N are outside the tensor map and not written; a block
-        // wholly past N (a cluster's spare row block) stores nothing
-        if (tid == 0 && mt * 128 < args.N)
+        // rows past N are outside the tensor map and not written
+        if (tid == 0)
           tma_store_3d(pc < 2 ? &tm_k : &tm_v, sb, (pc & 1) * 64, h, mt * 128);
       }
       // k_pe is shared by every head: the block's 128 rows x 64 rope values,
@@ -228,85 +203,11 @@ expand_kernel(const __grid_constant__ CUtensorMap tm_a,
     tc_fence_before();
   }
   __syncthreads();
-  // no CTA leaves while a peer may still multicast into it or arrive on it
-  if (CL > 1) cluster_sync();
   if (threadIdx.x == 0 && *abort_flag) raise_error(err, MLA_DEVERR_TIMEOUT);
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
-}
-
-template <int CL>
-cudaError_t launch_expand(int clusters, const CUtensorMap &ta, const CUtensorMap &tb,
-                          const CUtensorMap &tk, const CUtensorMap &tv, const ExpandArgs &a,
-                          int *err, cudaStream_t stream) {
-  cudaError_t e = cudaFuncSetAttribute(expand_kernel<CL>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters * CL);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, expand_kernel<CL>, ta, tb, tk, tv, a, err);
-}
-
-// Clusters of CL CTAs the device keeps resident at once (0 if none).
-template <int CL>
-int resident_clusters() {
-  if (cudaFuncSetAttribute(expand_kernel<CL>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           kSmemBytes) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(CL);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = kSmemBytes;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CL;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, expand_kernel<CL>, &cfg) != cudaSuccess) n = 0;
-  cudaGetLastError();   // a failed query leaves no sticky error behind
-  return n;
-}
-
-// The cluster size for this device: of 4, 2 and 1, the one whose resident
-// clusters cover the most SMs, the larger on a tie (cached per device).  On
-// a 152-SM GB300, 36 clusters of 4 (144 SMs) or 76 of 2 stay resident:
-// clusters of 2 (1.16 PFLOP/s at the DeepSeek-V3 context shape, the same as
-// without a cluster; clusters of 4 on 144 SMs: 1.08).
-struct ExpandShape {
-  int cl, clusters;
-};
-ExpandShape expand_shape() {
-  constexpr int kMaxDevices = 64;
-  static ExpandShape cache[kMaxDevices] = {};
-  static std::mutex mu;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return {1, 0};
-  const int sms = device_sm_count();
-  std::lock_guard<std::mutex> lock(mu);
-  if (dev >= 0 && dev < kMaxDevices && cache[dev].clusters > 0) return cache[dev];
-  ExpandShape sh{1, sms};
-  const int c4 = resident_clusters<4>(), c2 = resident_clusters<2>();
-  if (c2 * 2 >= sh.cl * sh.clusters && c2 > 0) sh = {2, c2};
-  if (c4 * 4 >= sh.cl * sh.clusters && c4 > 0) sh = {4, c4};
-  if (dev >= 0 && dev < kMaxDevices) cache[dev] = sh;
-  return sh;
 }
 
 }  // namespace
@@ -324,8 +225,6 @@ extern "C" int mla_expand_kv(const void *kv_rows, const void *w_kvb, int N,
     return MLA_ERR_INVALID_ARG;
   int *err = device_error_word();
   if (!err) return MLA_ERR_CUDA;
-  const ExpandShape sh = expand_shape();
-  if (sh.clusters < 1) return MLA_ERR_CUDA;
   CUtensorMap ta, tb;
   {
     const uint64_t dims[2] = {kDqk, static_cast<uint64_t>(N)};
@@ -338,8 +237,7 @@ extern "C" int mla_expand_kv(const void *kv_rows, const void *w_kvb, int N,
   {
     const uint64_t dims[2] = {kLatent, static_cast<uint64_t>(H) * 256};
     const uint64_t strides[1] = {kLatent * 2};
-    // each CTA of a cluster fetches 256 / CL rows of a head's 256
-    const uint32_t box[2] = {64, static_cast<uint32_t>(256 / sh.cl)};
+    const uint32_t box[2] = {64, 256};
     if (!make_tmap(&tb, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, w_kvb, dims, strides,
                    box, CU_TENSOR_MAP_SWIZZLE_128B))
       return MLA_ERR_CUDA;
@@ -367,14 +265,15 @@ extern "C" int mla_expand_kv(const void *kv_rows, const void *w_kvb, int N,
   a.N = N;
   a.H = H;
   a.m_tiles = (N + 127) / 128;
-  a.tiles = ((a.m_tiles + sh.cl - 1) / sh.cl) * H;
+  a.tiles = a.m_tiles * H;
   a.kv = static_cast<const __nv_bfloat16 *>(kv_rows);
   a.k_out = static_cast<__nv_bfloat16 *>(k_out);
-  const int clusters = a.tiles < sh.clusters ? a.tiles : sh.clusters;
-  cudaError_t e;
-  if (sh.cl == 4) e = launch_expand<4>(clusters, ta, tb, tk, tv, a, err, stream);
-  else if (sh.cl == 2) e = launch_expand<2>(clusters, ta, tb, tk, tv, a, err, stream);
-  else e = launch_expand<1>(clusters, ta, tb, tk, tv, a, err, stream);
-  if (e != cudaSuccess) return MLA_ERR_CUDA;
+  const int sms = device_sm_count();
+  if (sms < 1) return MLA_ERR_CUDA;
+  if (cudaFuncSetAttribute(expand_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           kSmemBytes) != cudaSuccess)
+    return MLA_ERR_CUDA;
+  const int grid = a.tiles < sms ? a.tiles : sms;
+  expand_kernel<<<grid, kThreads, kSmemBytes, stream>>>(ta, tb, tk, tv, a, err);
   return launch_status();
 }

@@ -104,19 +104,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map,
       : "memory");
 }
 
-// The same load delivered to the same shared-memory offset in every CTA of
-// the cluster named in `cta_mask`; each of them receives the transaction
-// bytes on its mbarrier at `bar`'s offset.  Source: this GPU's memory.
-__device__ __forceinline__ void tma_load_2d_multicast(void *dst, const CUtensorMap *map,
-                                                      uint64_t *bar, int x, int y,
-                                                      uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
-
 // L2 policy for data read once (evict it before anything else).
 __device__ __forceinline__ uint64_t l2_evict_first_policy() {
   uint64_t p;
@@ -329,15 +316,6 @@ __device__ __forceinline__ void mma_commit(uint64_t *bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 "
       "[%0];" ::"r"(smem_u32(bar))
-      : "memory");
-}
-
-// mma_commit, arriving on the mbarrier at `bar`'s offset in every CTA of the
-// cluster named in `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t *bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_u32(bar)), "h"(cta_mask)
       : "memory");
 }
 
