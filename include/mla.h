@@ -349,6 +349,23 @@ int mla_prefill_attn(const void *q, const void *k, const void *v,
                      int Nk, int H, int max_q_len, int causal, float sm_scale,
                      void *out, float *lse, mla_stream_t stream);
 
+/* ---------------------------------------------------------------------
+ * Host staging of a step's inputs and results
+ * [BLOG] §MLA Prefill vs Decode (each decode step takes the new tokens'
+ * queries in and hands the attention output on).  No page defines the
+ * transfer itself.
+ * Copies `bytes` from src to dst, where exactly one of the two is
+ * page-locked, device-mapped HOST memory (cudaHostAlloc / cudaHostRegister,
+ * e.g. a pinned torch tensor) and the other is memory of the current
+ * device; the SMs load and store over the host link (no copy engine), so
+ * the call is a kernel launch like every other entry point (asynchronous on
+ * `stream`, capturable in a CUDA graph; it waits for the previous kernel in
+ * the stream before reading src).  Both pointers 16-byte aligned, bytes a
+ * multiple of 16.  bytes == 0 is a no-op.
+ * Pageable host memory, host-to-host, device-to-device or another device's
+ * memory: MLA_ERR_INVALID_ARG, nothing launched. */
+int mla_stage_copy(void *dst, const void *src, size_t bytes, mla_stream_t stream);
+
 #ifdef __cplusplus
 } /* extern "C" */
 #endif

@@ -23,6 +23,7 @@ __all__ = [
     "mla_absorb_q", "mla_decode_workspace_size", "mla_decode_paged",
     "mla_decode_plan", "mla_merge_states", "mla_v_up", "mla_gather_cache",
     "mla_gather_cache_reorg", "mla_expand_kv", "mla_prefill_attn", "mla_rope_cache_write",
+    "mla_stage_copy",
 ]
 
 BF16, E4M3, F32 = 0, 1, 2
@@ -51,6 +52,7 @@ _SIGNATURES = {
     "mla_expand_kv": ([_p, _p, _i, _i, _p, _p, _p], _i),
     "mla_prefill_attn": ([_p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _p, _p, _p], _i),
     "mla_rope_cache_write": ([_p, _p, _p, _p, _p, _i, _i, _f, _i, _p, _i, _f, _i, _p], _i),
+    "mla_stage_copy": ([_p, _p, _sz, _p], _i),
 }
 
 
@@ -345,3 +347,24 @@ def mla_rope_cache_write(q_pe, k_pe, kv_c, positions, slot_mapping, kv_cache, *,
         _ptr(q_pe), _ptr(k_pe), _ptr(kv_c), _ptr(positions), _ptr(slot_mapping), T, H,
         float(rope_base), _ROPE_LAYOUT[layout], _ptr(kv_cache), _DTYPE_CODE[kv_cache.dtype],
         float(k_scale), kv_cache.shape[0], _stream()))
+
+
+def mla_stage_copy(dst, src):
+    """Copies src into dst (same byte size, both contiguous): exactly one of
+    them a CUDA tensor of the current device, the other a pinned CPU tensor.
+    The library's SMs move the bytes over the host link.  Returns dst."""
+    for t, name in ((dst, "dst"), (src, "src")):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a tensor")
+        if not t.is_contiguous():
+            raise ValueError(f"{name} must be contiguous")
+    if dst.is_cuda == src.is_cuda:
+        raise ValueError("exactly one of dst, src must be a CUDA tensor")
+    host = src if dst.is_cuda else dst
+    if not host.is_pinned():
+        raise ValueError("the host tensor must be pinned (page-locked)")
+    nbytes = dst.numel() * dst.element_size()
+    if nbytes != src.numel() * src.element_size():
+        raise ValueError("dst and src differ in size")
+    _check("mla_stage_copy", lib.mla_stage_copy(_ptr(dst), _ptr(src), nbytes, _stream()))
+    return dst

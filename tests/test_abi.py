@@ -95,6 +95,12 @@ def test_host_validation_rejects_bad_arguments():
                                   None, 0, 1.0, 1, s) == 1
     assert L.mla_rope_cache_write(None, None, None, None, None, 0, 0, 10000.0, 0,
                                   None, 0, 1.0, 1, s) == 0
+    # host staging: null pointers, a size that is not a multiple of 16, an
+    # unaligned pointer; zero bytes is a no-op
+    assert L.mla_stage_copy(None, None, 16, s) == 1
+    assert L.mla_stage_copy(ctypes.c_void_p(4096), ctypes.c_void_p(8192), 24, s) == 1
+    assert L.mla_stage_copy(ctypes.c_void_p(4100), ctypes.c_void_p(8192), 16, s) == 1
+    assert L.mla_stage_copy(None, None, 0, s) == 0
 
 
 def test_workspace_size_grows_with_work():
