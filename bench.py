@@ -405,7 +405,8 @@ def run_extras(device, flush, reps=10, only=None):
     decode and its chunked-prefill context step, and the rotary embedding +
     cache write of one decode step.  Inputs are seeded and synthetic.
     `only` (long, fp8, spec, prefill or rope) runs just that one, e.g. for a
-    profiler."""
+    profiler; `only` = gather or merge runs just that stage of the context
+    step (a few hundred MB on the device instead of the whole step's GB)."""
     want = lambda name: only is None or only == name
     import mla_latent_kv_uk_gb300 as m
     import synth
@@ -544,6 +545,39 @@ def run_extras(device, flush, reps=10, only=None):
         ex["prefill_ctx_4x8192_w4_sq512_h128"] = ex_p
         del caches, rows, kc, vc, kn, vn, oc, on, po, pl, mo, ml
 
+    # single stages of the context step, for a profiler: the gather + reorg
+    # of the 4 x 8192 context rows, and the final merge of the two states
+    # (synthetic states of the step's shape: 2048 new tokens x 128 heads)
+    if only == "gather":
+        cp = synth.context_prefill()
+        smb = max(s_[1].shape[1] for s_ in cp.shards)
+        tables = []
+        for _, sbt, _ in cp.shards:
+            t_ = np.full((cp.B, smb), -1, np.int32)
+            t_[:, :sbt.shape[1]] = sbt
+            tables.append(i32(t_))
+        caches = [s_[0].to(device) for s_ in cp.shards]
+        cu_c = np.concatenate([[0], np.cumsum(cp.ctx_lens)]).astype(np.int32)
+        dcu_c, Nc = i32(cu_c), int(cu_c[-1])
+        rows = torch.empty((Nc, 576), dtype=torch.bfloat16, device=device)
+        fn = lambda: m.mla_gather_cache_reorg(caches, tables, dcu_c, Nc, interleave=1, out=rows)
+        fn()
+        ex["gather_reorg_ctx_4x8192_w4"] = _roof(_timed_call(fn, flush, stream, reps),
+                                                 2 * Nc * 1152, 0, hbm, bf16, "bf16 measured")
+    if only == "merge":
+        cp = synth.context_prefill()
+        Tq, Hp = int(np.sum(cp.new_lens)), cp.H
+        g = torch.Generator(device="cpu").manual_seed(77)
+        po = torch.randn((2, Tq, Hp, 128), generator=g).to(torch.bfloat16).to(device)
+        pl = (torch.randn((2, Tq, Hp), generator=g) * 2.0 + 8.0).to(device)
+        mo = torch.empty((Tq, Hp, 128), dtype=torch.bfloat16, device=device)
+        ml = torch.empty((Tq, Hp), dtype=torch.float32, device=device)
+        fn = lambda: m.mla_merge_states(po, pl, out_dtype=torch.bfloat16, out=mo, out_lse=ml)
+        fn()
+        ex["merge_ctx_2048q_h128"] = _roof(_timed_call(fn, flush, stream, reps),
+                                           Tq * Hp * (3 * 128 * 2 + 3 * 4), 0, hbm, bf16,
+                                           "bf16 measured")
+
     # rotary embedding + cache write of one decode step at the DeepSeek-V3
     # shape (32 new tokens, 128 query heads)
     if want("rope"):
@@ -614,7 +648,8 @@ def main():
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the other workloads' timings (long request, fp8, spec decode, "
                          "prefill context step, rope + cache write)")
-    ap.add_argument("--only-extra", choices=["long", "fp8", "spec", "prefill", "rope"],
+    ap.add_argument("--only-extra", choices=["long", "fp8", "spec", "prefill", "rope", "gather",
+                                             "merge"],
                     help="time just that one of the other workloads and print its line "
                          "(for a profiler); no main bench")
     args = ap.parse_args()
