@@ -44,7 +44,7 @@ typedef struct CUstream_st *mla_stream_t; /* identical to cudaStream_t */
 enum mla_status {
   MLA_OK = 0,
   MLA_ERR_INVALID_ARG = 1, /* bad pointer / size / dtype combination        */
-  MLA_ERR_UNSUPPORTED = 2, /* valid request this build does not implement   */
+  MLA_ERR_UNSUPPORTED = 2, /* valid request the library does not implement */
   MLA_ERR_WORKSPACE = 3,   /* workspace missing or smaller than required    */
   MLA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed          */
 };
