@@ -190,6 +190,36 @@ def test_decode_causal_pair(m):
     _check(out, lse, *_oracle_decode(case))
 
 
+def test_decode_max_q_len(m):
+    """The largest q_len the call takes (64 causal query tokens per request):
+    token i of request b sees seq_len - 64 + i + 1 keys, so the first token
+    of the short request sees a single key and its last token all 64."""
+    case = synth.decode_case("qlen64", 443, B=2, H=128, seq_lens=[64, 700], q_len=64,
+                             poison=True)
+    out, lse = _run_decode(m, case)
+    ro, rl, t = _oracle_decode(case)
+    # a token that sees one or a few keys outputs (nearly) a raw value row,
+    # |o| up to ~5, where the bf16 rounding of the output alone (half an
+    # ulp, 2^-8 relative) exceeds 1e-2: the max-abs bound gets that
+    # documented term; the elementwise bound is unchanged
+    _check(out, lse, ro, rl, t, out_tol=OUT_TOL + 2.0 ** -8 * float(np.abs(ro).max()),
+           label="q_len 64")
+    assert m.mla_get_device_error() == 0
+
+
+def test_decode_max_heads(m):
+    """The largest head count the call takes (H = 4096: 32 head groups of
+    128, each its own job), over a ragged pair of requests."""
+    case = synth.decode_case("h4096", 444, B=2, H=4096, seq_lens=[300, 65], poison=True)
+    out, lse = _run_decode(m, case)
+    ro, rl, t = _oracle_decode(case)
+    # 4.2M outputs reach |o| where the bf16 rounding of the output alone
+    # exceeds 1e-2: the documented 2^-8 |o| term, elementwise bound unchanged
+    _check(out, lse, ro, rl, t, out_tol=OUT_TOL + 2.0 ** -8 * float(np.abs(ro).max()),
+           label="H 4096")
+    assert m.mla_get_device_error() == 0
+
+
 def test_decode_explicit_shards_then_merge(m):
     """Tiny decode shape: 2 shards per request via kv_starts/kv_ends, merged by
     mla_merge_states, equals the unsplit decode."""
