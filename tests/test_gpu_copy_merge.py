@@ -118,7 +118,14 @@ def test_reorg_bit_exact(m, W, I, kv_dtype, out_dtype):
     (2, 3, 16, 512, torch.float32, torch.bfloat16),
     (8, 1, 128, 512, torch.float32, torch.bfloat16),
     (3, 5, 7, 128, torch.bfloat16, torch.float32),
-    (1, 2, 4, 64, torch.float32, torch.float32)])
+    (1, 2, 4, 64, torch.float32, torch.float32),
+    # an odd number of 16-byte chunks per row (one chunk a thread), the
+    # smallest row, and the warp-per-row form past eight parts up to the
+    # largest part count the call takes
+    (2, 3, 3, 24, torch.bfloat16, torch.bfloat16),
+    (5, 2, 3, 8, torch.float32, torch.bfloat16),
+    (12, 2, 5, 512, torch.bfloat16, torch.bfloat16),
+    (256, 1, 2, 64, torch.float32, torch.float32)])
 def test_merge_states(m, S, T, H, D, pdt, odt):
     g = synth.generator(320 + S)
     po = torch.from_numpy(g.standard_normal((S, T, H, D)).astype(np.float32)).to(pdt)
