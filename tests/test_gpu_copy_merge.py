@@ -81,7 +81,8 @@ def test_gather_flags_bad_ranges(m):
 
 @pytest.mark.parametrize("W,I,kv_dtype,out_dtype", [
     (4, 1, "bf16", "bf16"), (2, 3, "bf16", "bf16"), (4, 1, "e4m3", "e4m3"),
-    (3, 2, "e4m3", "bf16"), (1, 1, "bf16", "bf16")])
+    (3, 2, "e4m3", "bf16"), (1, 1, "bf16", "bf16"),
+    (16, 1, "bf16", "bf16"), (16, 5, "e4m3", "bf16")])   # the most shards the call takes
 def test_reorg_bit_exact(m, W, I, kv_dtype, out_dtype):
     g = synth.generator(310 + W * 7 + I)
     ctx = np.array([1, 9, 64, 257, 1000], np.int32)
